@@ -1,0 +1,137 @@
+/*
+ * bam_attn.h - C ABI of the GB300 (sm_103a) GGD-BAM attention library.
+ *
+ * The method: Bayesian Attention Mechanism with a Generalized-Gaussian
+ * positional prior ("Bayesian Attention Mechanism" technical summary,
+ * gist.science 2505.22842, section "Solution Proposee : GGD-BAM").  Every
+ * query-key logit of head h gets the additive bias
+ *
+ *     b_h(d) = -( u / alpha_h )^beta_h,   u = |d - mu_h|,   d = i - j,
+ *
+ * with u clamped to max(u, eps) when beta_h <= 0 (the eps of the BAM
+ * repository README, "Implementation Details", eps = 1e-5).  Logits are
+ *
+ *     z_ij = c_i * q_i . k_j + b_h(i - j),
+ *     c_i  = 1/sqrt(D)                           (ssmax == 0)
+ *     c_i  = s_h * ln(n_i) / sqrt(D)             (ssmax != 0, Scalable-Softmax)
+ *
+ * where n_i is the number of keys query i sees (i+1 causal, T otherwise,
+ * Tkv for decode).  The output is softmax_j(z_ij) applied to V ("ALiBi:
+ * Attention with Linear Biases", section "Code": scores, softmax, weights @ V).
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are dense, row-major, in device memory, 16-byte aligned:
+ *    q, k, v, o, dO, dq, dk, dv are [B, H, T, D]; lse is [B, H, T].
+ *    bf16 tensors hold IEEE bfloat16 bit patterns.
+ *  - D must be 64 (other head sizes return BAM_ERR_UNSUPPORTED).
+ *  - The caller owns every buffer.  The library allocates nothing: scratch
+ *    space is the caller's workspace `ws` of at least
+ *    bam_attn_workspace_size(op, ...) bytes, 256-byte aligned.  A workspace
+ *    may be reused by calls that do not overlap on the GPU.
+ *  - Calls are asynchronous on `stream`.  Argument errors are returned
+ *    before anything is launched; launch failures return BAM_ERR_CUDA.
+ *  - Every on-device wait is bounded.  A kernel that gives up records
+ *    BAM_ERR_TIMEOUT in the workspace status word and returns; read it with
+ *    bam_attn_check_status().
+ */
+#ifndef BAM_ATTN_H_
+#define BAM_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BAM_OK = 0,
+  BAM_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer      */
+  BAM_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. D != 64)        */
+  BAM_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed            */
+  BAM_ERR_TIMEOUT = 4,     /* a device-side wait gave up (see check_status)   */
+  BAM_ERR_WORKSPACE = 5    /* workspace missing, misaligned or too small      */
+} bam_status;
+
+/* Per-head prior and SSMax parameters.  alpha, beta, mu, s point to device
+ * fp32 arrays of length H.  alpha_h > 0.  s is read only when ssmax != 0.
+ * eps is the clamp of |d - mu| used when beta_h <= 0 (README: 1e-5). */
+typedef struct {
+  const float* alpha;
+  const float* beta;
+  const float* mu;
+  const float* s;
+  float eps;
+  int causal; /* 1: key j visible to query i iff j <= i; 0: all keys visible */
+  int ssmax;  /* 1: Scalable-Softmax logit scale s_h * ln(n_i)               */
+} bam_params;
+
+enum { BAM_OP_FWD = 0, BAM_OP_BWD = 1, BAM_OP_DECODE = 2 };
+
+/* Bytes of workspace that op (BAM_OP_*) needs for these sizes (T = Tkv for
+ * decode).  Returns 0 for invalid sizes.  Host-only; launches nothing. */
+size_t bam_attn_workspace_size(int op, int B, int H, int T, int D);
+
+/* Forward (prefill).  q, k, v: bf16 [B,H,T,D].  o: [B,H,T,D], fp32 when
+ * o_fp32 != 0, else bf16.  lse: fp32 [B,H,T] natural-log log-sum-exp of the
+ * logits of each row (may be NULL; bam_attn_bwd needs it).  T >= 1.
+ * Steps: per-head distance table b_h(d) (fp64 math, fp32 store) into ws, then
+ * the fused tiled kernel (tensor-core QK^T and PV, online softmax). */
+bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, int o_fp32,
+                        float* lse, int B, int H, int T, int D, const bam_params* p,
+                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Backward of L = sum(O * dO) ("plain chain rule"; the pages give no
+ * backward).  q, k, v, dO: bf16 [B,H,T,D]; o and lse: the forward's outputs
+ * (o fp32 when o_fp32 != 0, else bf16).  Outputs: dq, dk, dv bf16
+ * [B,H,T,D]; dalpha, dbeta, dmu, ds fp32 [H], overwritten, summed over the
+ * batch (ds is written as 0 when ssmax == 0). */
+bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        int o_fp32, const float* lse, const void* dO, void* dq, void* dk,
+                        void* dv, float* dalpha, float* dbeta, float* dmu, float* ds, int B,
+                        int H, int T, int D, const bam_params* p, void* ws, size_t ws_bytes,
+                        cudaStream_t stream);
+
+/* Decode: one new query per (b, h) against a KV cache that already holds
+ * its key and value.  q: bf16 [B,H,D]; kc, vc: bf16 [B,H,Tkv,D].  The query
+ * sits at position Tkv-1, every cached key is visible and n = Tkv.
+ * o: [B,H,D] fp32 when o_fp32 != 0, else bf16; lse: fp32 [B,H] or NULL.
+ * p->causal is ignored.  Split-KV partials go to ws. */
+bam_status bam_attn_decode(const void* q, const void* kc, const void* vc, void* o, int o_fp32,
+                           float* lse, int B, int H, int Tkv, int D, const bam_params* p,
+                           void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * `ws`.  Returns BAM_OK, BAM_ERR_TIMEOUT (a device wait gave up) or
+ * BAM_ERR_CUDA. */
+bam_status bam_attn_check_status(void* ws, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* bam_status_string(bam_status s);
+
+/* Kernels that bam_attn_profile_events can bracket. */
+enum {
+  BAM_KERNEL_TABLE = 0,      /* distance-table kernel (fwd, bwd, decode)   */
+  BAM_KERNEL_FWD = 1,        /* fused forward                               */
+  BAM_KERNEL_BWD_PREP = 2,   /* backward preprocess (Delta, zeroing)        */
+  BAM_KERNEL_BWD = 3,        /* fused backward                              */
+  BAM_KERNEL_BWD_FINAL = 4,  /* dq conversion and scalar-gradient finish    */
+  BAM_KERNEL_DECODE = 5,     /* split-KV decode                             */
+  BAM_KERNEL_DECODE_COMBINE = 6,
+  BAM_KERNEL_COUNT = 7
+};
+
+/* Instrumentation: while set, every launch of kernel `which` is bracketed
+ * by cudaEventRecord(before) / cudaEventRecord(after) on the launch stream.
+ * Pass NULL events to clear.  Not thread-safe with concurrent callers. */
+bam_status bam_attn_profile_events(int which, cudaEvent_t before, cudaEvent_t after);
+
+/* Number of kernel launches the library has issued since load (all kinds). */
+uint64_t bam_attn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BAM_ATTN_H_ */

@@ -1,0 +1,51 @@
+"""Shared helpers for the GPU parity tests (device upload, oracle inputs)."""
+
+import numpy as np
+import torch
+
+from transformer_attention_ggd_gb300.inputs import bf16_bits, bf16_to_f64
+
+# Tolerances: O is compared in fp32 output mode with a max-abs bound of 1e-2;
+# gradients (dq, dk, dv) and the per-head scalar gradients with a relative
+# bound of 2e-2 (relative to the largest reference magnitude of the tensor;
+# for a scalar, to max(|g|, 1e-2 * sum of |per-element terms|)).
+O_ATOL = 1e-2
+GRAD_RTOL = 2e-2
+# LSE is not bounded by the method's stated tolerances.  Logits are fp32 dot
+# products of bf16 inputs plus an fp32 table value, so LSE carries the fp32
+# representation error of the logit itself (relative ~6e-8; an eps-clamped
+# bias can reach -1e6) plus the bf16 rounding of the weights in the row sum
+# (relative 2^-9 per weight, averaging out): 2e-3 absolute + 1e-6 relative.
+LSE_ATOL = 2e-3
+LSE_RTOL = 1e-6
+
+
+def dev_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(
+        torch.bfloat16)
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def dev_f32(x, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(device)
+
+
+def normal_bits(rng, shape) -> np.ndarray:
+    return bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+
+
+def params_dev(prm):
+    return {n: dev_f32(prm[n]) for n in ("alpha", "beta", "mu", "s")}
+
+
+def f64(bits):
+    return bf16_to_f64(bits)
+
+
+def scalar_rel_err(got, ref, absg):
+    den = np.maximum(np.abs(ref), 1e-2 * absg)
+    den = np.where(den == 0, 1.0, den)
+    return np.abs(got - ref) / den

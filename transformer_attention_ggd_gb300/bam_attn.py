@@ -1,0 +1,237 @@
+"""Thin ctypes binding of the C ABI in include/bam_attn.h.
+
+Argument marshalling only: torch tensors supply device pointers and the
+current CUDA stream; every step of the computation runs in the CUDA kernels
+of libbam_attn.so.  There is no fallback: if the library is missing or no
+GPU is present, calls raise.
+
+The functions carry the C names (bam_attn_fwd, bam_attn_bwd, ...).  The
+helpers at the bottom (``attention_forward`` and friends) allocate outputs
+and workspace with torch and then call the same entry points.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libbam_attn.so")
+
+BAM_OK = 0
+BAM_ERR_INVALID_ARG = 1
+BAM_ERR_UNSUPPORTED = 2
+BAM_ERR_CUDA = 3
+BAM_ERR_TIMEOUT = 4
+BAM_ERR_WORKSPACE = 5
+
+BAM_OP_FWD, BAM_OP_BWD, BAM_OP_DECODE = 0, 1, 2
+
+BAM_KERNEL_TABLE = 0
+BAM_KERNEL_FWD = 1
+BAM_KERNEL_BWD_PREP = 2
+BAM_KERNEL_BWD = 3
+BAM_KERNEL_BWD_FINAL = 4
+BAM_KERNEL_DECODE = 5
+BAM_KERNEL_DECODE_COMBINE = 6
+BAM_KERNEL_COUNT = 7
+
+# Every symbol that include/bam_attn.h declares.
+EXPORTED = (
+    "bam_attn_workspace_size",
+    "bam_attn_fwd",
+    "bam_attn_bwd",
+    "bam_attn_decode",
+    "bam_attn_check_status",
+    "bam_status_string",
+    "bam_attn_profile_events",
+    "bam_attn_launch_count",
+)
+
+
+class BamError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bam_status_string(status)} (status {status})")
+
+
+class BamParams(ctypes.Structure):
+    _fields_ = [
+        ("alpha", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p),
+        ("mu", ctypes.c_void_p),
+        ("s", ctypes.c_void_p),
+        ("eps", ctypes.c_float),
+        ("causal", ctypes.c_int),
+        ("ssmax", ctypes.c_int),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libbam_attn.so and declare its signatures (no GPU needed)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        pp = ctypes.POINTER(BamParams)
+        lib.bam_attn_workspace_size.restype = sz
+        lib.bam_attn_workspace_size.argtypes = [i, i, i, i, i]
+        lib.bam_attn_fwd.restype = i
+        lib.bam_attn_fwd.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp, sz, vp]
+        lib.bam_attn_bwd.restype = i
+        lib.bam_attn_bwd.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     i, i, i, i, pp, vp, sz, vp]
+        lib.bam_attn_decode.restype = i
+        lib.bam_attn_decode.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp, sz, vp]
+        lib.bam_attn_check_status.restype = i
+        lib.bam_attn_check_status.argtypes = [vp, vp]
+        lib.bam_status_string.restype = ctypes.c_char_p
+        lib.bam_status_string.argtypes = [i]
+        lib.bam_attn_profile_events.restype = i
+        lib.bam_attn_profile_events.argtypes = [i, vp, vp]
+        lib.bam_attn_launch_count.restype = ctypes.c_uint64
+        lib.bam_attn_launch_count.argtypes = []
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------- raw entry points
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_params(alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False) -> BamParams:
+    """alpha, beta, mu, s: float32 CUDA tensors of length H (kept alive by the caller)."""
+    return BamParams(alpha.data_ptr(), beta.data_ptr(), mu.data_ptr(),
+                     s.data_ptr() if s is not None else None, float(eps), int(bool(causal)),
+                     int(bool(ssmax)))
+
+
+def _check(status: int, where: str):
+    if status != BAM_OK:
+        raise BamError(status, where)
+
+
+def bam_status_string(status: int) -> str:
+    return load_library().bam_status_string(int(status)).decode()
+
+
+def bam_attn_workspace_size(op: int, B: int, H: int, T: int, D: int = 64) -> int:
+    return int(load_library().bam_attn_workspace_size(op, B, H, T, D))
+
+
+def bam_attn_fwd(q, k, v, o, lse, params: BamParams, ws, stream=None) -> None:
+    import torch
+    B, H, T, D = q.shape
+    o_fp32 = 1 if o.dtype == torch.float32 else 0
+    st = load_library().bam_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), o_fp32, _ptr(lse), B, H,
+                                     T, D, ctypes.byref(params), _ptr(ws), ws.numel(),
+                                     _stream(stream))
+    _check(st, "bam_attn_fwd")
+
+
+def bam_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, dalpha, dbeta, dmu, ds, params: BamParams,
+                 ws, stream=None) -> None:
+    import torch
+    B, H, T, D = q.shape
+    o_fp32 = 1 if o.dtype == torch.float32 else 0
+    st = load_library().bam_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), o_fp32, _ptr(lse),
+                                     _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
+                                     _ptr(dbeta), _ptr(dmu), _ptr(ds), B, H, T, D,
+                                     ctypes.byref(params), _ptr(ws), ws.numel(),
+                                     _stream(stream))
+    _check(st, "bam_attn_bwd")
+
+
+def bam_attn_decode(q, kc, vc, o, lse, params: BamParams, ws, stream=None) -> None:
+    import torch
+    B, H, Tkv, D = kc.shape
+    o_fp32 = 1 if o.dtype == torch.float32 else 0
+    st = load_library().bam_attn_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(o), o_fp32, _ptr(lse),
+                                        B, H, Tkv, D, ctypes.byref(params), _ptr(ws), ws.numel(),
+                                        _stream(stream))
+    _check(st, "bam_attn_decode")
+
+
+def bam_attn_check_status(ws, stream=None) -> int:
+    return int(load_library().bam_attn_check_status(_ptr(ws), _stream(stream)))
+
+
+def bam_attn_profile_events(which: int, before=None, after=None) -> None:
+    b = ctypes.c_void_p(before.cuda_event) if before is not None else None
+    a = ctypes.c_void_p(after.cuda_event) if after is not None else None
+    _check(load_library().bam_attn_profile_events(which, b, a), "bam_attn_profile_events")
+
+
+def bam_attn_launch_count() -> int:
+    return int(load_library().bam_attn_launch_count())
+
+
+# ---------------------------------------------------------------- allocating helpers
+
+def workspace(op: int, B: int, H: int, T: int, device="cuda"):
+    import torch
+    n = bam_attn_workspace_size(op, B, H, T, 64)
+    if n == 0:
+        raise BamError(BAM_ERR_INVALID_ARG, "bam_attn_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def attention_forward(q, k, v, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False,
+                      o_dtype=None, ws=None, stream=None):
+    """q, k, v: bf16 [B,H,T,64] CUDA tensors -> (o, lse)."""
+    import torch
+    B, H, T, D = q.shape
+    o = torch.empty((B, H, T, D), dtype=o_dtype or torch.float32, device=q.device)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(BAM_OP_FWD, B, H, T, q.device)
+    prm = make_params(alpha, beta, mu, s, eps, causal, ssmax)
+    bam_attn_fwd(q, k, v, o, lse, prm, ws, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dO, alpha, beta, mu, s=None, eps=1e-5, causal=True,
+                       ssmax=False, ws=None, stream=None):
+    """Returns dq, dk, dv (bf16) and dalpha, dbeta, dmu, ds (fp32 [H])."""
+    import torch
+    B, H, T, D = q.shape
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    g = [torch.empty(H, dtype=torch.float32, device=q.device) for _ in range(4)]
+    if ws is None:
+        ws = workspace(BAM_OP_BWD, B, H, T, q.device)
+    prm = make_params(alpha, beta, mu, s, eps, causal, ssmax)
+    bam_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, g[0], g[1], g[2], g[3], prm, ws, stream)
+    return dq, dk, dv, g[0], g[1], g[2], g[3]
+
+
+def attention_decode(q, kc, vc, alpha, beta, mu, s=None, eps=1e-5, ssmax=False, o_dtype=None,
+                     ws=None, stream=None):
+    """q: bf16 [B,H,64]; kc, vc: bf16 [B,H,Tkv,64] -> (o [B,H,64], lse [B,H])."""
+    import torch
+    B, H, Tkv, D = kc.shape
+    o = torch.empty((B, H, D), dtype=o_dtype or torch.float32, device=q.device)
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(BAM_OP_DECODE, B, H, Tkv, q.device)
+    prm = make_params(alpha, beta, mu, s, eps, True, ssmax)
+    bam_attn_decode(q, kc, vc, o, lse, prm, ws, stream)
+    return o, lse

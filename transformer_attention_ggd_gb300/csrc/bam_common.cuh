@@ -1,0 +1,123 @@
+// Definitions shared by the kernels and the host entry points of the GGD-BAM
+// attention library: workspace layout, distance-table geometry, kernel
+// argument blocks and the internal launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "bam_ptx.cuh"
+
+namespace bam {
+
+constexpr int kHeadDim = 64;
+constexpr double kLog2e = 1.4426950408889634074;
+constexpr float kLn2f = 0.69314718055994530942f;
+
+// Workspace: [0, 256) device status words, then op-specific regions, each
+// 256-byte aligned.
+constexpr size_t kStatusBytes = 256;
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Per-head distance table (forward / backward): entry x of head h holds
+// b_h(d) * log2(e) for d = x - off.  Entries exist for every d that a
+// 128 x 256 tile window can touch; all windows start at a multiple of 128
+// entries, so their byte offsets are 512-byte aligned.
+struct TableGeom {
+  int off;  // index of d = 0
+  int len;  // entries per head, multiple of 256
+};
+
+inline TableGeom table_geom(int T, int causal) {
+  const int t256 = ((T + 255) / 256) * 256;
+  const int off = causal ? 256 : t256 + 256;
+  return TableGeom{off, off + t256 + 256};
+}
+
+// Decode table: entry j of head h holds b_h(Tkv - 1 - j) * log2(e) for the
+// key at cache position j (0 beyond Tkv); rows padded to 64 entries.
+inline int decode_table_len(int Tkv) { return ((Tkv + 63) / 64) * 64; }
+
+enum TableMode : int {
+  kTableByDistance = 0,  // forward: b only
+  kTableDecode = 1,      // decode: by key position
+  kTableBackward = 2     // backward: b, db/dbeta, db/dmu (three tables)
+};
+
+struct TableArgs {
+  float* tab;  // [ntables][H][len]
+  const float* alpha;
+  const float* beta;
+  const float* mu;
+  DevStatus* status;  // zeroed by block 0 (the first kernel of every call)
+  float eps;
+  int H, len, off, Tkv, mode;
+};
+
+struct FwdArgs {
+  void* o;
+  float* lse;
+  const float* table;
+  const float* s;
+  DevStatus* status;
+  int B, H, T, nqb;
+  int causal, ssmax, o_fp32;
+  int tab_len, tab_off;
+};
+
+struct DecodeArgs {
+  const uint16_t* q;   // [BH, 64]
+  const uint16_t* kc;  // [BH, Tkv, 64]
+  const uint16_t* vc;
+  const float* table;  // [H, tab_len]
+  const float* s;
+  float* part;         // [BH, nsplit, 2 + 64]: m (log2 units), l, o[64]
+  void* o;
+  float* lse;
+  DevStatus* status;
+  int B, H, Tkv, nsplit, chunk, tab_len;
+  int ssmax, o_fp32;
+};
+
+struct BwdArgs {
+  const void* o;        // forward output (fp32 or bf16)
+  const uint16_t* dO;   // bf16
+  const float* lse;     // natural-log LSE from the forward
+  const float* table;   // [3][H][len]: b*log2e, db/dbeta, db/dmu
+  const float* alpha;
+  const float* beta;
+  const float* s;
+  float* delta;         // [BH, T]: rowsum(dO * O)
+  float* dq_acc;        // [BH, T, 64] fp32
+  float* gacc;          // [4][H] fp32: sum dS*b, sum dS*db/dbeta, sum dS*db/dmu, sum dS*ln(n)qk/sqrt(D)
+  uint16_t* dq;         // bf16 outputs
+  uint16_t* dk;
+  uint16_t* dv;
+  float* dalpha;
+  float* dbeta;
+  float* dmu;
+  float* ds;
+  DevStatus* status;
+  int B, H, T, nkb;
+  int causal, ssmax, o_fp32;
+  int tab_len, tab_off;
+};
+
+// Internal launchers (one per kernel).  Each returns the launch error.
+cudaError_t launch_table(const TableArgs& a, cudaStream_t st);
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st);
+
+// Decode split geometry.
+void decode_split(int BH, int Tkv, int* nsplit, int* chunk);
+
+}  // namespace bam

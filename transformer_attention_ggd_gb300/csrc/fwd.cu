@@ -1,0 +1,405 @@
+// Fused GGD-BAM attention forward for sm_103a (tcgen05 / TMEM / TMA).
+//
+// Computes, per (b, h) and query row i,
+//   z_ij = c_i * q_i . k_j + b_h(i - j),   O_i = softmax_j(z_ij) V,
+//   LSE_i = log sum_j exp(z_ij),
+// with c_i = 1/sqrt(D) or, with Scalable-Softmax, s_h ln(n_i)/sqrt(D)
+// ("Bayesian Attention Mechanism" summary, "Solution Proposee : GGD-BAM" for
+// the bias and SSMax; "ALiBi: Attention with Linear Biases", "Code" for
+// scores -> softmax -> weights @ V).  The bias comes from the per-head
+// distance table (table.cu), staged per key tile into shared memory by a
+// bulk copy, so no power function runs per element.
+//
+// One CTA owns 256 query rows of one (b, h) as two 128-row tiles A and B and
+// walks the key/value tiles of 128 keys:
+//   warp 8      TMA producer: Q once; per key tile K, V and the 384-entry
+//               distance window, into a 3-stage ring.
+//   warp 9      MMA issuer (one thread): S_t = Q_t K^T (128x128x64, both
+//               operands K-major in shared memory) and O_t += P_t V (P from
+//               Tensor Memory, V MN-major), accumulators in Tensor Memory.
+//               Also allocates / frees the 512 TMEM columns.
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B: one thread
+//               per query row reads its S row from TMEM, adds c_i S + bias in
+//               log2 units, runs the online softmax (exp2, rescaling O in
+//               TMEM only when the running max grows by more than 8), writes
+//               P (bf16) back to TMEM, and in the end normalises O.
+// The two softmax groups are offset by one MMA so the tensor core works on
+// one tile while the other is in its softmax.
+//
+// TMEM columns: S_A [0,128) S_B [128,256) P_A [256,320) P_B [320,384)
+//               O_A [384,448) O_B [448,512).
+#include "bam_common.cuh"
+
+namespace bam {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kThreads = 320;  // 10 warps: 168 registers per thread at most
+constexpr int kTileBytes = 128 * 64 * 2;
+constexpr int kWin = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct __align__(1024) FwdSmem {
+  uint8_t q[2][kTileBytes];
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+  float win[kStages][kWin];
+  uint64_t q_full;
+  uint64_t k_full[kStages];
+  uint64_t v_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t mma_final;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Sites recorded in the status word when a wait gives up.
+enum : int {
+  kSiteProducer = 10,
+  kSiteMmaQ = 20,
+  kSiteMmaK = 21,
+  kSiteMmaV = 22,
+  kSiteMmaSFree = 23,
+  kSiteMmaP = 24,
+  kSiteSoftS = 30,
+  kSiteSoftK = 31,
+  kSiteSoftPV = 32,
+  kSiteSoftEnd = 33
+};
+
+// All lanes wait; the result is made warp-uniform so that the collective
+// tcgen05.ld/st that follow are executed by the whole warp or by none of it.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, DevStatus* st,
+                                          volatile int* ab, int site) {
+  const bool ok = mbar_wait(bar, parity, st, ab, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void store_row(const FwdArgs& a, int64_t row, const uint32_t* ov,
+                                          float inv_l) {
+  if (a.o_fp32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + row * kHeadDim);
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      dst[x] = make_float4(__uint_as_float(ov[4 * x]) * inv_l,
+                           __uint_as_float(ov[4 * x + 1]) * inv_l,
+                           __uint_as_float(ov[4 * x + 2]) * inv_l,
+                           __uint_as_float(ov[4 * x + 3]) * inv_l);
+    }
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + row * kHeadDim);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(ov[8 * x + 0]) * inv_l, __uint_as_float(ov[8 * x + 1]) * inv_l);
+      w.y = pack_bf16x2(__uint_as_float(ov[8 * x + 2]) * inv_l, __uint_as_float(ov[8 * x + 3]) * inv_l);
+      w.z = pack_bf16x2(__uint_as_float(ov[8 * x + 4]) * inv_l, __uint_as_float(ov[8 * x + 5]) * inv_l);
+      w.w = pack_bf16x2(__uint_as_float(ov[8 * x + 6]) * inv_l, __uint_as_float(ov[8 * x + 7]) * inv_l);
+      dst[x] = w;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bam_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work item: causal blocks with the most key tiles go first.
+  const int BH = a.B * a.H;
+  const int qb = a.causal ? (a.nqb - 1 - static_cast<int>(blockIdx.x) / BH)
+                          : static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int h = bh % a.H;
+  const int i0 = qb * 256;
+  const int nkv = (a.T + 127) / 128;
+  const int qt = i0 / 128;
+  const bool hasB = i0 + 128 < a.T;
+  const int nA = a.causal ? min(qt + 1, nkv) : nkv;
+  const int nB = hasB ? (a.causal ? min(qt + 2, nkv) : nkv) : 0;
+  const int nKV = max(nA, nB);
+  volatile int* ab = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = *reinterpret_cast<volatile int*>(&a.status->abort);
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.s_free[t], 4);
+      mbar_init(&sm.p_full[t], 4);
+      mbar_init(&sm.pv_done[t], 1);
+    }
+    mbar_init(&sm.mma_final, 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = sm.tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = (*ab == 0);
+      int issued = 0;
+      bool q_issued = false;
+      if (ok) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        mbar_arrive_expect_tx(&sm.q_full, kTileBytes * (hasB ? 2 : 1));
+        tma_load_3d(sm.q[0], &tq, &sm.q_full, 0, i0, bh);
+        if (hasB) tma_load_3d(sm.q[1], &tq, &sm.q_full, 0, i0 + 128, bh);
+        q_issued = true;
+      }
+      // Window of key tile j starts at d = i0 - 128 - 128 j.
+      const float* tab_h = a.table + static_cast<size_t>(h) * a.tab_len + a.tab_off + i0 - 128;
+      for (int j = 0; ok && j < nKV; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages) {
+          ok = mbar_wait(&sm.kv_empty[s], ((j / kStages) - 1) & 1, a.status, ab, kSiteProducer);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes + kWin * 4);
+        tma_load_3d(sm.k[s], &tk, &sm.k_full[s], 0, 128 * j, bh);
+        bulk_load(sm.win[s], tab_h - 128 * j, kWin * 4, &sm.k_full[s]);
+        mbar_arrive_expect_tx(&sm.v_full[s], kTileBytes);
+        tma_load_3d(sm.v[s], &tv, &sm.v_full[s], 0, 128 * j, bh);
+        issued = j + 1;
+      }
+      // Copies still in flight land before this CTA leaves.
+      if (q_issued) mbar_drain(&sm.q_full, 0);
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        mbar_drain(&sm.k_full[j % kStages], (j / kStages) & 1);
+        mbar_drain(&sm.v_full[j % kStages], (j / kStages) & 1);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = (*ab == 0);
+      const uint32_t idS = idesc_bf16(128, 128, false, false);
+      const uint32_t idO = idesc_bf16(128, 64, false, true);
+      auto issue_S = [&](int t, int s) {
+        const uint32_t qa = smem_u32(sm.q[t]);
+        const uint32_t ka = smem_u32(sm.k[s]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ss(tm + 128 * t, sdesc_sw128(qa + 32 * kk, 16, 1024),
+                  sdesc_sw128(ka + 32 * kk, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        umma_commit(&sm.s_full[t]);
+      };
+      auto issue_PV = [&](int t, int s, int j) {
+        const uint32_t va = smem_u32(sm.v[s]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tm + 384 + 64 * t, tm + 256 + 64 * t + 8 * kk,
+                  sdesc_sw128(va + 2048 * kk, 16384, 1024), idO, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&sm.pv_done[t]);
+      };
+      if (ok) ok = mbar_wait(&sm.q_full, 0, a.status, ab, kSiteMmaQ);
+      if (ok) ok = mbar_wait(&sm.k_full[0], 0, a.status, ab, kSiteMmaK);
+      if (ok) {
+        tc_fence_after();
+        if (nA > 0) issue_S(0, 0);
+        if (nB > 0) issue_S(1, 0);
+      }
+      for (int j = 0; ok && j < nKV; ++j) {
+        const int s = j % kStages;
+        if (j + 1 < nKV) {
+          ok = mbar_wait(&sm.k_full[(j + 1) % kStages], ((j + 1) / kStages) & 1, a.status, ab,
+                         kSiteMmaK);
+          if (!ok) break;
+        }
+        ok = mbar_wait(&sm.v_full[s], (j / kStages) & 1, a.status, ab, kSiteMmaV);
+        if (!ok) break;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int nt = t ? nB : nA;
+          if (j >= nt) continue;
+          if (j + 1 < nt) {
+            ok = mbar_wait(&sm.s_free[t], j & 1, a.status, ab, kSiteMmaSFree);
+            if (!ok) break;
+            tc_fence_after();
+            issue_S(t, (j + 1) % kStages);
+          }
+          ok = mbar_wait(&sm.p_full[t], j & 1, a.status, ab, kSiteMmaP);
+          if (!ok) break;
+          tc_fence_after();
+          issue_PV(t, s, j);
+        }
+        if (!ok) break;
+        umma_commit(&sm.kv_empty[s]);
+      }
+      // Everything issued has completed before Tensor Memory is released.
+      umma_commit(&sm.mma_final);
+      mbar_drain(&sm.mma_final, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;                 // 0: tile A, 1: tile B
+    const int r = threadIdx.x - 128 * t;     // row within the tile = TMEM lane
+    const int i = i0 + 128 * t + r;          // query position
+    const int nt = t ? nB : nA;
+    const uint32_t lb = tmem_lane_base(warp);
+    const uint32_t tS = tm + lb + 128 * t;
+    const uint32_t tP = tm + lb + 256 + 64 * t;
+    const uint32_t tO = tm + lb + 384 + 64 * t;
+    float cr;  // logit scale in log2 units
+    {
+      const float n = a.causal ? static_cast<float>(i + 1) : static_cast<float>(a.T);
+      const float c = a.ssmax ? __ldg(a.s + h) * logf(n) * 0.125f : 0.125f;
+      cr = c * 1.44269504088896341f;
+    }
+    float m = -INFINITY, l = 0.0f;
+    bool ok = (*ab == 0);
+    const int woff = 128 * (t + 1) + r;  // window index of column 0
+    for (int j = 0; ok && j < nt; ++j) {
+      const int s = j % kStages;
+      ok = warp_wait(&sm.s_full[t], j & 1, a.status, ab, kSiteSoftS);
+      if (!ok) break;
+      ok = warp_wait(&sm.k_full[s], (j / kStages) & 1, a.status, ab, kSiteSoftK);
+      if (!ok) break;
+      tc_fence_after();
+      // S row -> z = c_i S + bias (log2 units), 32 columns at a time; the
+      // next chunk's TMEM load overlaps this chunk's arithmetic.
+      const float* wv = sm.win[s] + woff;
+      float z[128];
+      uint32_t sr[2][32];
+      tmem_ld_32x32b_x32(tS, sr[0]);
+      tmem_ld_wait();
+      reg_fence32(sr[0]);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        if (ch < 3) tmem_ld_32x32b_x32(tS + 32 * (ch + 1), sr[(ch + 1) & 1]);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          z[32 * ch + c] = fmaf(__uint_as_float(sr[ch & 1][c]), cr, wv[-(32 * ch + c)]);
+        if (ch < 3) {
+          tmem_ld_wait();
+          reg_fence32(sr[(ch + 1) & 1]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.s_free[t]);
+
+      const int j0 = 128 * j;
+      const bool tail = j0 + 128 > a.T;
+      const bool diag = a.causal && (j0 + 127 > i0 + 128 * t);
+      if (diag || tail) {
+        int lim = a.T - 1 - j0;
+        if (a.causal) lim = min(lim, i - j0);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) z[c] = -INFINITY;
+      }
+      float mx = z[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, z[c]);
+      const float m_new = fmaxf(m, mx);
+      const bool resc = m_new > m + kRescaleThreshold;
+      float scale = 1.0f;
+      if (resc) {
+        scale = ex2_approx(m - m_new);
+        l *= scale;
+        m = m_new;
+      }
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(z[2 * c] - m);
+        const float p1 = ex2_approx(z[2 * c + 1] - m);
+        const uint32_t w = pack_bf16x2(p0, p1);
+        pk[c] = w;
+        // The row sum adds the bf16-rounded weights that the PV product
+        // uses, so O is an exact weighted average of V under those weights.
+        l += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+      }
+      if (j > 0) {
+        // PV of the previous tile must be done: frees P and makes O stable.
+        ok = warp_wait(&sm.pv_done[t], (j - 1) & 1, a.status, ab, kSiteSoftPV);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st_32x32b_x32(tP, pk);
+      tmem_st_32x32b_x32(tP + 32, pk + 32);
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        uint32_t ov[64];
+        tmem_ld_32x32b_x32(tO, ov);
+        tmem_ld_32x32b_x32(tO + 32, ov + 32);
+        tmem_ld_wait();
+        reg_fence32(ov);
+        reg_fence32(ov + 32);
+#pragma unroll
+        for (int x = 0; x < 64; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * scale);
+        tmem_st_32x32b_x32(tO, ov);
+        tmem_st_32x32b_x32(tO + 32, ov + 32);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full[t]);
+    }
+    if (ok && nt > 0) {
+      ok = warp_wait(&sm.pv_done[t], (nt - 1) & 1, a.status, ab, kSiteSoftEnd);
+      if (ok) {
+        tc_fence_after();
+        uint32_t ov[64];
+        tmem_ld_32x32b_x32(tO, ov);
+        tmem_ld_32x32b_x32(tO + 32, ov + 32);
+        tmem_ld_wait();
+        reg_fence32(ov);
+        reg_fence32(ov + 32);
+        if (i < a.T) {
+          const int64_t row = static_cast<int64_t>(bh) * a.T + i;
+          store_row(a, row, ov, 1.0f / l);
+          if (a.lse) a.lse[row] = (m + __log2f(l)) * kLn2f;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tm, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(FwdSmem) + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(bam_fwd_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const unsigned grid = static_cast<unsigned>(a.nqb) * static_cast<unsigned>(a.B * a.H);
+  bam_fwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace bam
