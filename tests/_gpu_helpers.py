@@ -7,10 +7,15 @@ from transformer_attention_ggd_gb300.inputs import bf16_bits, bf16_to_f64
 
 # Tolerances: O is compared in fp32 output mode with a max-abs bound of 1e-2;
 # gradients (dq, dk, dv) and the per-head scalar gradients with a relative
-# bound of 2e-2 (relative to the largest reference magnitude of the tensor;
-# for a scalar, to max(|g|, 1e-2 * sum of |per-element terms|)).
+# bound of 2e-2.  "Relative" for a tensor: max|g - g*| / max(max|g*|, 1e-3);
+# for a scalar: |g - g*| / max(|g*|, 1e-2 * sum of |per-element terms|, 1e-4).
+# The floors only matter where the reference vanishes (T = 1 has dS = 0
+# exactly; far heads contribute ~1e-14), so that fp32 noise is not divided by
+# zero.
 O_ATOL = 1e-2
 GRAD_RTOL = 2e-2
+GRAD_FLOOR = 1e-3
+SCALAR_FLOOR = 1e-4
 # LSE is not bounded by the method's stated tolerances.  Logits are fp32 dot
 # products of bf16 inputs plus an fp32 table value, so LSE carries the fp32
 # representation error of the logit itself (relative ~6e-8; an eps-clamped
@@ -46,6 +51,9 @@ def f64(bits):
 
 
 def scalar_rel_err(got, ref, absg):
-    den = np.maximum(np.abs(ref), 1e-2 * absg)
-    den = np.where(den == 0, 1.0, den)
+    den = np.maximum(np.maximum(np.abs(ref), 1e-2 * absg), SCALAR_FLOOR)
     return np.abs(got - ref) / den
+
+
+def tensor_rel_err(got, ref):
+    return np.abs(got - ref).max() / max(np.abs(ref).max(), GRAD_FLOOR)

@@ -1,11 +1,565 @@
-// Backward launchers (kernels follow).
+// Fused GGD-BAM attention backward for sm_103a (tcgen05 / TMEM / TMA).
+//
+// The pages give no backward; this is the chain rule of L = sum(O * dO)
+// through the forward of fwd.cu:
+//   P_ij  = exp(z_ij - LSE_i),  z_ij = c_i q_i.k_j + b_h(i - j)
+//   dP_ij = dO_i . v_j,  Delta_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - Delta_i)
+//   dV_j += sum_i P_ij dO_i,  dK_j += sum_i c_i dS_ij q_i,  dQ_i += sum_j c_i dS_ij k_j
+//   dalpha_h = -(beta_h/alpha_h) sum dS b,  dbeta_h = sum dS db/dbeta,
+//   dmu_h = sum dS db/dmu,  ds_h = sum dS ln(n_i) q_i.k_j / sqrt(D)   (SSMax)
+// with db/dbeta and db/dmu read from the distance tables written by table.cu.
+//
+// Delta_i is taken from the forward's O, which carries the bf16 rounding of
+// the weights in its PV product (or a bf16 output).  That error enters each
+// scalar-gradient sum as -dDelta_i * sum_j P_ij X_ij without cancelling, so
+// the kernel also accumulates, per row, B_i = sum_j P_ij X_ij and the exact
+// C_i = sum_j P_ij dP_ij, and the final kernel adds sum_i (Delta_i - C_i) B_i:
+//   sum_ij P_ij (dP_ij - C_i) X_ij = sum_ij dS_ij X_ij + sum_i (Delta_i - C_i) B_i.
+//
+// One CTA owns a 128-key tile of one (b, h) and walks the 128-row query
+// tiles that see it:
+//   warp 4     TMA producer: K, V once; per query tile Q, dO and the three
+//              256-entry distance windows (b, db/dbeta, db/dmu), 2 stages.
+//   warp 5     MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
+//              dV += P^T dO and dK += (c dS)^T Q (A operands MN-major in shared
+//              memory, M = keys) and dQ = (c dS) K (A = c dS from TMEM).
+//   warps 0-3  one thread per query row: P, dS, the four scalar-gradient
+//              sums, P and c*dS to shared memory and c*dS to TMEM, then the
+//              dQ tile added to an fp32 accumulator with vector reductions.
+//              At the end, dK and dV rows (TMEM lane = key) go out as bf16.
+// TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
+//               dK [384,448) dV [448,512).
 #include "bam_common.cuh"
 
 namespace bam {
-cudaError_t launch_bwd_prep(const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_bwd(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                       const CUtensorMap&, const BwdArgs&, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int kBStages = 2;
+constexpr int kBThreads = 192;
+constexpr int kTile = 128 * 64 * 2;  // 16 KB bf16 tile
+constexpr int kBWin = 256;
+
+struct __align__(1024) BwdSmem {
+  uint8_t k[kTile];
+  uint8_t v[kTile];
+  uint8_t q[kBStages][kTile];
+  uint8_t dO[kBStages][kTile];
+  uint8_t pt[2 * kTile];   // P^T as an MN-major A operand: 2 atoms of 64 keys x 128 queries
+  uint8_t dst[2 * kTile];  // (c dS)^T, same layout
+  float win[kBStages][3][kBWin];
+  float red[4][4];
+  uint64_t kv_full;
+  uint64_t qd_full[kBStages];
+  uint64_t qd_empty[kBStages];
+  uint64_t s_full;
+  uint64_t ds_ready;
+  uint64_t mma_done;
+  uint64_t mma_final;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+enum : int {
+  kSiteBProd = 50,
+  kSiteBMmaKV = 60,
+  kSiteBMmaQD = 61,
+  kSiteBMmaDS = 62,
+  kSiteBWgS = 70,
+  kSiteBWgQD = 71,
+  kSiteBWgDone = 72
+};
+
+constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 320, kColDK = 384,
+                   kColDV = 448;
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, DevStatus* st,
+                                          volatile int* ab, int site) {
+  const bool ok = mbar_wait(bar, parity, st, ab, site);
+  return __all_sync(0xffffffffu, ok);
 }
-cudaError_t launch_bwd_final(const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+// Byte offset of element (m, k) of a 128 x 128 bf16 MN-major operand
+// (m = key, contiguous; k = query) in the 128-byte-swizzled layout: atoms of
+// 64 m-values; within an atom, row k at (k/8)*1024 + (k%8)*128 and the
+// 16-byte chunk m/8 swizzled with k%8.
+__device__ __forceinline__ uint32_t mn_chunk_offset(int m8, int k) {
+  // m8: index of the 8-key chunk (0..15)
+  return (m8 >> 3) * kTile + (k >> 3) * 1024 + (k & 7) * 128 + (((m8 & 7) ^ (k & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kBThreads, 1)
+    bam_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                   const BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int BH = a.B * a.H;
+  const int kb = static_cast<int>(blockIdx.x) / BH;  // causal: most query tiles first
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int h = bh % a.H;
+  const int j0 = kb * 128;
+  const int nqt = (a.T + 127) / 128;
+  const int q_first = a.causal ? kb : 0;
+  const int nq = nqt - q_first;
+  volatile int* ab = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = *reinterpret_cast<volatile int*>(&a.status->abort);
+    mbar_init(&sm.kv_full, 1);
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(&sm.qd_full[s], 1);
+      mbar_init(&sm.qd_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.ds_ready, 4);
+    mbar_init(&sm.mma_done, 1);
+    mbar_init(&sm.mma_final, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = sm.tmem_base;
+  const size_t plane = static_cast<size_t>(a.H) * a.tab_len;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = (*ab == 0);
+      bool kv_issued = false;
+      int issued = 0;
+      if (ok) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        prefetch_tmap(&tdo);
+        mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
+        tma_load_3d(sm.k, &tk, &sm.kv_full, 0, j0, bh);
+        tma_load_3d(sm.v, &tv, &sm.kv_full, 0, j0, bh);
+        kv_issued = true;
+      }
+      for (int t = 0; ok && t < nq; ++t) {
+        const int s = t % kBStages;
+        const int i0 = (q_first + t) * 128;
+        if (t >= kBStages) {
+          ok = mbar_wait(&sm.qd_empty[s], ((t / kBStages) - 1) & 1, a.status, ab, kSiteBProd);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTile + 3 * kBWin * 4);
+        tma_load_3d(sm.q[s], &tq, &sm.qd_full[s], 0, i0, bh);
+        tma_load_3d(sm.dO[s], &tdo, &sm.qd_full[s], 0, i0, bh);
+        const size_t base = static_cast<size_t>(h) * a.tab_len + a.tab_off + i0 - j0 - 128;
+        for (int p = 0; p < 3; ++p)
+          bulk_load(sm.win[s][p], a.table + p * plane + base, kBWin * 4, &sm.qd_full[s]);
+        issued = t + 1;
+      }
+      if (kv_issued) mbar_drain(&sm.kv_full, 0);
+      for (int t = max(0, issued - kBStages); t < issued; ++t)
+        mbar_drain(&sm.qd_full[t % kBStages], (t / kBStages) & 1);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = (*ab == 0);
+      const uint32_t idSP = idesc_bf16(128, 128, false, false);
+      const uint32_t idKV = idesc_bf16(128, 64, true, true);
+      const uint32_t idQ = idesc_bf16(128, 64, false, true);
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+      const uint32_t pta = smem_u32(sm.pt), dsa = smem_u32(sm.dst);
+      auto issue_s_dp = [&](int s) {
+        const uint32_t qa = smem_u32(sm.q[s]), da = smem_u32(sm.dO[s]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ss(tm + kColS, sdesc_sw128(qa + 32 * kk, 16, 1024),
+                  sdesc_sw128(ka + 32 * kk, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ss(tm + kColDP, sdesc_sw128(da + 32 * kk, 16, 1024),
+                  sdesc_sw128(va + 32 * kk, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+        umma_commit(&sm.s_full);
+      };
+      if (ok) ok = mbar_wait(&sm.kv_full, 0, a.status, ab, kSiteBMmaKV);
+      if (ok && nq > 0) ok = mbar_wait(&sm.qd_full[0], 0, a.status, ab, kSiteBMmaQD);
+      if (ok && nq > 0) {
+        tc_fence_after();
+        issue_s_dp(0);
+      }
+      for (int t = 0; ok && t < nq; ++t) {
+        const int s = t % kBStages;
+        ok = mbar_wait(&sm.ds_ready, t & 1, a.status, ab, kSiteBMmaDS);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sm.q[s]), da = smem_u32(sm.dO[s]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
+          umma_ss(tm + kColDV, sdesc_sw128(pta + 2048 * kk, kTile, 1024),
+                  sdesc_sw128(da + 2048 * kk, kTile, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dK += (c dS)^T Q
+          umma_ss(tm + kColDK, sdesc_sw128(dsa + 2048 * kk, kTile, 1024),
+                  sdesc_sw128(qa + 2048 * kk, kTile, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ = (c dS) K
+          umma_ts(tm + kColDQ, tm + kColDS + 8 * kk, sdesc_sw128(ka + 2048 * kk, kTile, 1024),
+                  idQ, kk > 0 ? 1u : 0u);
+        umma_commit(&sm.mma_done);
+        umma_commit(&sm.qd_empty[s]);
+        if (t + 1 < nq) {
+          ok = mbar_wait(&sm.qd_full[(t + 1) % kBStages], ((t + 1) / kBStages) & 1, a.status, ab,
+                         kSiteBMmaQD);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s_dp((t + 1) % kBStages);
+        }
+      }
+      umma_commit(&sm.mma_final);
+      mbar_drain(&sm.mma_final, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ element-wise
+    const int r = threadIdx.x;  // query row within the tile = TMEM lane
+    const uint32_t lb = tmem_lane_base(warp);
+    const float s_h = a.ssmax ? __ldg(a.s + h) : 1.0f;
+    float acc_b = 0.f, acc_beta = 0.f, acc_mu = 0.f, acc_s = 0.f;
+    bool ok = (*ab == 0);
+    auto dq_epilogue = [&](int t) {
+      const int i = (q_first + t) * 128 + r;
+      uint32_t dv[64];
+      tmem_ld_32x32b_x32(tm + lb + kColDQ, dv);
+      tmem_ld_32x32b_x32(tm + lb + kColDQ + 32, dv + 32);
+      tmem_ld_wait();
+      reg_fence32(dv);
+      reg_fence32(dv + 32);
+      if (i < a.T) {
+        float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.T + i) * kHeadDim;
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          red_add_v4(dst + 4 * x, __uint_as_float(dv[4 * x]), __uint_as_float(dv[4 * x + 1]),
+                     __uint_as_float(dv[4 * x + 2]), __uint_as_float(dv[4 * x + 3]));
+      }
+    };
+    for (int t = 0; ok && t < nq; ++t) {
+      const int s = t % kBStages;
+      const int i0 = (q_first + t) * 128;
+      const int i = i0 + r;
+      const bool row_ok = i < a.T;
+      // Per-row constants.
+      const float n = a.causal ? static_cast<float>(i + 1) : static_cast<float>(a.T);
+      const float w_ln = logf(n) * 0.125f;             // ln(n_i)/sqrt(D)
+      const float cn = a.ssmax ? s_h * w_ln : 0.125f;   // c_i
+      const float cr = cn * 1.44269504088896341f;      // c_i log2(e)
+      const size_t ridx = static_cast<size_t>(bh) * a.T + i;
+      const float lse2 = row_ok ? __ldg(a.lse + ridx) * 1.44269504088896341f : INFINITY;
+      const float delta = row_ok ? __ldg(a.delta + ridx) : 0.0f;
+      int lim = a.T - 1 - j0;              // last visible key column
+      if (a.causal) lim = min(lim, i - j0);
+      const bool need_mask = lim < 127;
+
+      ok = warp_wait(&sm.s_full, t & 1, a.status, ab, kSiteBWgS);
+      if (!ok) break;
+      ok = warp_wait(&sm.qd_full[s], (t / kBStages) & 1, a.status, ab, kSiteBWgQD);
+      if (!ok) break;
+      if (t > 0) {
+        // Previous tile's MMAs are done: P^T / dS^T buffers and dS TMEM are
+        // free, and its dQ tile is ready.
+        ok = warp_wait(&sm.mma_done, (t - 1) & 1, a.status, ab, kSiteBWgDone);
+        if (!ok) break;
+        tc_fence_after();
+        dq_epilogue(t - 1);
+      }
+      tc_fence_after();
+      const float* wb = sm.win[s][0] + 128 + r;
+      const float* wbeta = sm.win[s][1] + 128 + r;
+      const float* wmu = sm.win[s][2] + 128 + r;
+      float row_ss = 0.f;
+      float pb = 0.f, pbeta = 0.f, pmu = 0.f, ps = 0.f, pdp = 0.f;  // sum_j P X, sum_j P dP
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sv[32], dpv[32];
+        tmem_ld_32x32b_x32(tm + lb + kColS + 32 * ch, sv);
+        tmem_ld_32x32b_x32(tm + lb + kColDP + 32 * ch, dpv);
+        tmem_ld_wait();
+        reg_fence32(sv);
+        reg_fence32(dpv);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 32 * ch + x + e;
+            const float sval = __uint_as_float(sv[x + e]);
+            const float tb = wb[-c];
+            float zz = fmaf(sval, cr, tb);
+            if (need_mask && c > lim) zz = -INFINITY;
+            const float p = ex2_approx(zz - lse2);
+            const float dpval = __uint_as_float(dpv[x + e]);
+            const float dS = p * (dpval - delta);
+            const float tbeta = wbeta[-c], tmu = wmu[-c];
+            acc_b = fmaf(dS, tb, acc_b);
+            acc_beta = fmaf(dS, tbeta, acc_beta);
+            acc_mu = fmaf(dS, tmu, acc_mu);
+            row_ss = fmaf(dS, sval, row_ss);
+            pb = fmaf(p, tb, pb);
+            pbeta = fmaf(p, tbeta, pbeta);
+            pmu = fmaf(p, tmu, pmu);
+            ps = fmaf(p, sval, ps);
+            pdp = fmaf(p, dpval, pdp);
+            pv[e] = p;
+            dsv[e] = dS * cn;
+          }
+          pp[x / 2] = pack_bf16x2(pv[0], pv[1]);
+          dd[x / 2] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // P and c*dS, keys [32ch, 32ch+32) of query row r, into the MN-major
+        // operands (four 16-byte chunks each) and c*dS into TMEM.
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const uint32_t off = mn_chunk_offset(4 * ch + q8, r);
+          *reinterpret_cast<uint4*>(sm.pt + off) =
+              make_uint4(pp[4 * q8], pp[4 * q8 + 1], pp[4 * q8 + 2], pp[4 * q8 + 3]);
+          *reinterpret_cast<uint4*>(sm.dst + off) =
+              make_uint4(dd[4 * q8], dd[4 * q8 + 1], dd[4 * q8 + 2], dd[4 * q8 + 3]);
+        }
+        tmem_st_32x32b_x16(tm + lb + kColDS + 16 * ch, dd);
+      }
+      acc_s = fmaf(row_ss, w_ln, acc_s);
+      if (row_ok) {
+        float* ra = a.rowacc + ridx * 8;
+        red_add_v4(ra, pb, pbeta, pmu, ps * w_ln);
+        red_add_v4(ra + 4, pdp, 0.f, 0.f, 0.f);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.ds_ready);
+    }
+    if (ok && nq > 0) {
+      ok = warp_wait(&sm.mma_done, (nq - 1) & 1, a.status, ab, kSiteBWgDone);
+      if (ok) {
+        tc_fence_after();
+        dq_epilogue(nq - 1);
+        // dK and dV rows: TMEM lane = key j0 + r.
+        const int j = j0 + r;
+        uint32_t kvv[64];
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col = which ? kColDV : kColDK;
+          tmem_ld_32x32b_x32(tm + lb + col, kvv);
+          tmem_ld_32x32b_x32(tm + lb + col + 32, kvv + 32);
+          tmem_ld_wait();
+          reg_fence32(kvv);
+          reg_fence32(kvv + 32);
+          if (j < a.T) {
+            uint16_t* out = (which ? a.dv : a.dk) + (static_cast<size_t>(bh) * a.T + j) * kHeadDim;
+            uint4* o4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              o4[x] = make_uint4(
+                  pack_bf16x2(__uint_as_float(kvv[8 * x]), __uint_as_float(kvv[8 * x + 1])),
+                  pack_bf16x2(__uint_as_float(kvv[8 * x + 2]), __uint_as_float(kvv[8 * x + 3])),
+                  pack_bf16x2(__uint_as_float(kvv[8 * x + 4]), __uint_as_float(kvv[8 * x + 5])),
+                  pack_bf16x2(__uint_as_float(kvv[8 * x + 6]), __uint_as_float(kvv[8 * x + 7])));
+          }
+        }
+      }
+    }
+    // Causal key tiles beyond every query contribute nothing; write their dK, dV.
+    if (ok && nq == 0) {
+      const int j = j0 + r;
+      if (j < a.T) {
+        uint4* k4 = reinterpret_cast<uint4*>(a.dk + (static_cast<size_t>(bh) * a.T + j) * kHeadDim);
+        uint4* v4 = reinterpret_cast<uint4*>(a.dv + (static_cast<size_t>(bh) * a.T + j) * kHeadDim);
+        for (int x = 0; x < 8; ++x) {
+          k4[x] = make_uint4(0, 0, 0, 0);
+          v4[x] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    // Block reduction of the scalar-gradient sums, one atomic per head and sum.
+    float v4[4] = {acc_b, acc_beta, acc_mu, acc_s};
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v4[x] += __shfl_xor_sync(0xffffffffu, v4[x], off);
+    if (lane == 0)
+      for (int x = 0; x < 4; ++x) sm.red[warp][x] = v4[x];
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (threadIdx.x < 4 && ok) {
+      const float tot = sm.red[0][threadIdx.x] + sm.red[1][threadIdx.x] +
+                        sm.red[2][threadIdx.x] + sm.red[3][threadIdx.x];
+      atomicAdd(a.gacc + threadIdx.x * a.H + h, tot);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tm, 512);
+  }
+}
+
+// Delta_i = dO_i . O_i; zero the dq accumulator and the scalar sums.
+__global__ void bam_bwd_prep_kernel(const BwdArgs a) {
+  const size_t rows = static_cast<size_t>(a.B) * a.H * a.T;
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t row = tid; row < rows; row += nthreads) {
+    const uint4* g = reinterpret_cast<const uint4*>(a.dO + row * kHeadDim);
+    float acc = 0.f;
+    if (a.o_fp32) {
+      const float4* o = reinterpret_cast<const float4*>(static_cast<const float*>(a.o) + row * kHeadDim);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const uint4 w = g[x];
+        const float4 o0 = o[2 * x], o1 = o[2 * x + 1];
+        acc += __uint_as_float(w.x << 16) * o0.x + __uint_as_float(w.x & 0xFFFF0000u) * o0.y +
+               __uint_as_float(w.y << 16) * o0.z + __uint_as_float(w.y & 0xFFFF0000u) * o0.w +
+               __uint_as_float(w.z << 16) * o1.x + __uint_as_float(w.z & 0xFFFF0000u) * o1.y +
+               __uint_as_float(w.w << 16) * o1.z + __uint_as_float(w.w & 0xFFFF0000u) * o1.w;
+      }
+    } else {
+      const uint4* o = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + row * kHeadDim);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const uint4 w = g[x], u = o[x];
+        acc += __uint_as_float(w.x << 16) * __uint_as_float(u.x << 16) +
+               __uint_as_float(w.x & 0xFFFF0000u) * __uint_as_float(u.x & 0xFFFF0000u) +
+               __uint_as_float(w.y << 16) * __uint_as_float(u.y << 16) +
+               __uint_as_float(w.y & 0xFFFF0000u) * __uint_as_float(u.y & 0xFFFF0000u) +
+               __uint_as_float(w.z << 16) * __uint_as_float(u.z << 16) +
+               __uint_as_float(w.z & 0xFFFF0000u) * __uint_as_float(u.z & 0xFFFF0000u) +
+               __uint_as_float(w.w << 16) * __uint_as_float(u.w << 16) +
+               __uint_as_float(w.w & 0xFFFF0000u) * __uint_as_float(u.w & 0xFFFF0000u);
+      }
+    }
+    a.delta[row] = acc;
+  }
+  float4* dq4 = reinterpret_cast<float4*>(a.dq_acc);
+  const size_t n4 = rows * (kHeadDim / 4);
+  for (size_t x = tid; x < n4; x += nthreads) dq4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4* ra4 = reinterpret_cast<float4*>(a.rowacc);
+  for (size_t x = tid; x < rows * 2; x += nthreads) ra4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid == 0) *a.counter = 0;
+  for (size_t x = tid; x < static_cast<size_t>(4 * a.H); x += nthreads) a.gacc[x] = 0.f;
+}
+
+// dq (bf16) from the fp32 accumulator; the Delta correction of the scalar
+// sums (row blocks of one (b, h) per CTA); the last CTA writes the per-head
+// scalar gradients.
+constexpr int kFinalRows = 2048;
+
+__global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
+  const size_t n8 = static_cast<size_t>(a.B) * a.H * a.T * (kHeadDim / 8);
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+  if (*reinterpret_cast<volatile int*>(&a.status->abort)) return;
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc);
+  uint4* dst = reinterpret_cast<uint4*>(a.dq);
+  for (size_t x = tid; x < n8; x += nthreads) {
+    const float4 u = src[2 * x], w = src[2 * x + 1];
+    dst[x] = make_uint4(pack_bf16x2(u.x, u.y), pack_bf16x2(u.z, u.w), pack_bf16x2(w.x, w.y),
+                        pack_bf16x2(w.z, w.w));
+  }
+  // Correction sum_i (Delta_i - C_i) B_i over this CTA's rows.
+  const int chunks = (a.T + kFinalRows - 1) / kFinalRows;
+  __shared__ float red[8][4];
+  __shared__ bool last;
+  for (int item = blockIdx.x; item < a.B * a.H * chunks; item += gridDim.x) {
+    const int bh = item / chunks;
+    const int r0 = (item % chunks) * kFinalRows;
+    const int r1 = min(a.T, r0 + kFinalRows);
+    float c4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = r0 + threadIdx.x; i < r1; i += blockDim.x) {
+      const size_t row = static_cast<size_t>(bh) * a.T + i;
+      const float4 bsum = reinterpret_cast<const float4*>(a.rowacc + row * 8)[0];
+      const float cexact = a.rowacc[row * 8 + 4];
+      const float dd = a.delta[row] - cexact;
+      c4[0] = fmaf(dd, bsum.x, c4[0]);
+      c4[1] = fmaf(dd, bsum.y, c4[1]);
+      c4[2] = fmaf(dd, bsum.z, c4[2]);
+      c4[3] = fmaf(dd, bsum.w, c4[3]);
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) c4[x] += __shfl_xor_sync(0xffffffffu, c4[x], off);
+    if ((threadIdx.x & 31) == 0)
+      for (int x = 0; x < 4; ++x) red[threadIdx.x >> 5][x] = c4[x];
+    __syncthreads();
+    if (threadIdx.x < 4) {
+      float tot = 0.f;
+      for (int w = 0; w < 8; ++w) tot += red[w][threadIdx.x];
+      atomicAdd(a.gacc + threadIdx.x * a.H + bh % a.H, tot);
+    }
+    __syncthreads();
+  }
+  // Last CTA: per-head outputs.
+  __threadfence();
+  if (threadIdx.x == 0) last = (atomicAdd(a.counter, 1) == static_cast<int>(gridDim.x) - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const volatile float* g = a.gacc;
+  for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
+    const float beta = a.beta[h], alpha = a.alpha[h];
+    // sum dS * b = ln(2) * sum dS * (b log2 e);  db/dalpha = -beta b / alpha
+    a.dalpha[h] = -(beta / alpha) * kLn2f * g[h];
+    a.dbeta[h] = g[a.H + h];
+    a.dmu[h] = g[2 * a.H + h];
+    a.ds[h] = a.ssmax ? g[3 * a.H + h] : 0.0f;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st) {
+  const size_t rows = static_cast<size_t>(a.B) * a.H * a.T;
+  const size_t want = (rows * 16 + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(want < 152 * 8 ? (want < 1 ? 1 : want) : 152 * 8);
+  bam_bwd_prep_kernel<<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(BwdSmem) + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(bam_bwd_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const unsigned grid = static_cast<unsigned>(a.nkb) * static_cast<unsigned>(a.B * a.H);
+  bam_bwd_kernel<<<grid, kBThreads, smem, st>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
+  const size_t n8 = static_cast<size_t>(a.B) * a.H * a.T * (kHeadDim / 8);
+  const size_t items = static_cast<size_t>(a.B) * a.H * ((a.T + kFinalRows - 1) / kFinalRows);
+  size_t want = (n8 + 255) / 256;
+  if (want < items) want = items;
+  if (want > 152 * 8) want = 152 * 8;
+  const unsigned grid = static_cast<unsigned>(want);
+  bam_bwd_final_kernel<<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace bam

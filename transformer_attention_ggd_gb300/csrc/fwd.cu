@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c = a.ssmax ? __ldg(a.s + h) * logf(n) * 0.125f : 0.125f;
       cr = c * 1.44269504088896341f;
     }
-    float m = -INFINITY, l = 0.0f;
+    float m = -INFINITY, l = 0.0f, le = 0.0f;
     bool ok = (*ab == 0);
     const int woff = 128 * (t + 1) + r;  // window index of column 0
     for (int j = 0; ok && j < nt; ++j) {
@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (resc) {
         scale = ex2_approx(m - m_new);
         l *= scale;
+        le *= scale;
         m = m_new;
       }
       uint32_t pk[64];
@@ -328,9 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float p1 = ex2_approx(z[2 * c + 1] - m);
         const uint32_t w = pack_bf16x2(p0, p1);
         pk[c] = w;
-        // The row sum adds the bf16-rounded weights that the PV product
-        // uses, so O is an exact weighted average of V under those weights.
+        // O is normalised by the sum of the bf16-rounded weights that the PV
+        // product uses (an exact weighted average of V under those weights);
+        // the LSE keeps the sum of the unrounded weights.
         l += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+        le += p0 + p1;
       }
       if (j > 0) {
         // PV of the previous tile must be done: frees P and makes O stable.
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < a.T) {
           const int64_t row = static_cast<int64_t>(bh) * a.T + i;
           store_row(a, row, ov, 1.0f / l);
-          if (a.lse) a.lse[row] = (m + __log2f(l)) * kLn2f;
+          if (a.lse) a.lse[row] = (m + __log2f(le)) * kLn2f;
         }
       }
     }
