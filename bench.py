@@ -1,0 +1,490 @@
+"""Benchmark of the GGD-BAM attention hot path on GB300.
+
+Default workload: the training step fwd+bwd at B=8, H=12, T=512, D=64,
+causal, BAM+SSMax (seeded synthetic bf16 tensors shaped like the pages'
+T=512 training runs).  A step is one forward and one backward through the C
+ABI (distance tables, fused forward, backward preprocess, fused backward,
+finalisation).  Throughput counts the algorithmic causal work: B*H*T(T+1)/2
+query-key pairs at 4*D flop (forward) + 10*D flop (backward) per pair.
+
+One JSON line on rank 0 with the device-timed value, the end-to-end value
+through host buffers, the roofline of the dominant kernel (timed live with
+the library's event hook), the fp64 CPU oracle as a baseline, the launch
+count and the SM clocks seen during the timed region.  Extra lines of the
+other workloads (long-context prefill, decode) are reported under "extra".
+
+--impl reference times the oracle (the method's plain fp64 statement) on the
+host cores on the same workload, bounded samples per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BAM attention causal fwd/bwd TFLOP/s and % of BF16 tensor peak; decode GB/s"
+D = 64
+
+
+def hook_events(torch, n):
+    """n (before, after) CUDA event pairs for the library's profiling hook.
+    torch creates the underlying event on the first record(), so record each
+    once here; the library then re-records them around its launches."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    return evs
+
+
+def pairs_causal(B, H, T):
+    return B * H * T * (T + 1) // 2
+
+
+def train_flops(B, H, T):
+    return pairs_causal(B, H, T) * (4 * D + 10 * D)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transformer_attention_ggd_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    entry = t.get(kernel)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def make_train_inputs(torch, dev, seed=None):
+    from transformer_attention_ggd_gb300.inputs import make_inputs
+    d = make_inputs(2, seed=seed)
+
+    def bf(b):
+        return torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    t = {n: bf(d[n]) for n in ("q", "k", "v", "do")}
+    for n in ("alpha", "beta", "mu", "s"):
+        t[n] = torch.from_numpy(d[n]).to(dev)
+    return d, t
+
+
+def run_ours(args, rank, world, dev, torch, dist):
+    from transformer_attention_ggd_gb300 import bam_attn as ba
+
+    ba.load_library()
+    peaks = load_peaks()
+    B, H, T = 8, 12, 512
+    d, t = make_train_inputs(torch, dev, seed=1002 + rank)
+    prm = ba.make_params(t["alpha"], t["beta"], t["mu"], t["s"], 1e-5, True, True)
+    o = torch.empty((B, H, T, D), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(t["q"]) for _ in range(3))
+    g = [torch.empty(H, dtype=torch.float32, device=dev) for _ in range(4)]
+    ws_f = ba.workspace(ba.BAM_OP_FWD, B, H, T, dev)
+    ws_b = ba.workspace(ba.BAM_OP_BWD, B, H, T, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
+
+    def step(q, k, v, do):
+        ba.bam_attn_fwd(q, k, v, o, lse, prm, ws_f, stream)
+        ba.bam_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, g[0], g[1], g[2], g[3], prm, ws_b,
+                        stream)
+
+    for _ in range(args.warmup):
+        step(t["q"], t["k"], t["v"], t["do"])
+    torch.cuda.synchronize()
+    if ba.bam_attn_check_status(ws_b) != ba.BAM_OK or ba.bam_attn_check_status(ws_f) != ba.BAM_OK:
+        raise RuntimeError("device status not clean after warm-up")
+
+    # Device-timed steps; L2 flushed between steps (outside the events).
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    kev = {k: hook_events(torch, args.steps) for k in (ba.BAM_KERNEL_FWD, ba.BAM_KERNEL_BWD)}
+    launches0 = ba.bam_attn_launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            for k, lst in kev.items():
+                ba.bam_attn_profile_events(k, lst[i][0], lst[i][1])
+            ev[i][0].record(stream)
+            step(t["q"], t["k"], t["v"], t["do"])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    for k in kev:
+        ba.bam_attn_profile_events(k, None, None)
+    launches = ba.bam_attn_launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    kern_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in lst) for k, lst in kev.items()}
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    flops_step = train_flops(B, H, T)
+    value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # End to end through the C ABI with host buffers: H2D of the step's
+    # inputs from pinned memory, fwd+bwd, D2H of the gradients, every step.
+    host_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
+    dev_in = {n: torch.empty_like(t[n]) for n in host_in}
+    host_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (dq, dk, dv)]
+    host_g = [torch.empty(H, dtype=torch.float32).pin_memory() for _ in range(4)]
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = sum(x.numel() * x.element_size() for x in host_out) + sum(x.numel() * 4 for x in host_g)
+
+    def e2e_step():
+        for n in host_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        step(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["do"])
+        for hst, src in zip(host_out + host_g, [dq, dk, dv] + g):
+            hst.copy_(src, non_blocking=True)
+
+    for _ in range(max(2, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_ms = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e_ms += e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e_ms = float(tt.item())
+    e2e_value = flops_step * args.steps * world / (e_ms * 1e-3) / 1e12
+
+    # Roofline of the dominant kernel (the fused backward): algorithmic
+    # flops of one launch (10 D per causal pair) over its mean duration.
+    bwd_flops = pairs_causal(B, H, T) * 10 * D
+    fwd_flops = pairs_causal(B, H, T) * 4 * D
+    dom = ba.BAM_KERNEL_BWD if kern_ms[ba.BAM_KERNEL_BWD] >= kern_ms[ba.BAM_KERNEL_FWD] \
+        else ba.BAM_KERNEL_FWD
+    dom_flops = bwd_flops if dom == ba.BAM_KERNEL_BWD else fwd_flops
+    achieved = dom_flops / (kern_ms[dom] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    roof = {"kernel": "bam_bwd_kernel" if dom == ba.BAM_KERNEL_BWD else "bam_fwd_kernel",
+            "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic("bam_bwd_kernel" if dom == ba.BAM_KERNEL_BWD
+                                        else "bam_fwd_kernel"),
+            "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
+            "kernel_ms": {"fwd": round(kern_ms[ba.BAM_KERNEL_FWD], 4),
+                          "bwd": round(kern_ms[ba.BAM_KERNEL_BWD], 4)},
+            "fwd_frac": round(fwd_flops / (kern_ms[ba.BAM_KERNEL_FWD] * 1e-3) / 1e12 / peak, 4)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 tensors and per-head parameters)",
+        "config": {"workload": "train_B8_H12_T512", "B": B, "H": H, "T": T, "D": D,
+                   "causal": True, "ssmax": True, "step": "fwd+bwd",
+                   "l2": "flushed (256 MB write) between timed steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    return line, t
+
+
+def extra_workloads(torch, dev, steps, peaks):
+    """Long-context prefill and decode (parity configurations), timed briefly."""
+    from transformer_attention_ggd_gb300 import bam_attn as ba
+    from transformer_attention_ggd_gb300.inputs import make_inputs
+
+    out = {}
+
+    def bf(b):
+        return torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    for cfg, reps in ((3, max(3, steps // 4)), (4, 2)):
+        d = make_inputs(cfg)
+        q, k, v = bf(d["q"]), bf(d["k"]), bf(d["v"])
+        p = {n: torch.from_numpy(d[n]).to(dev) for n in ("alpha", "beta", "mu", "s")}
+        B, H, T = d["B"], d["H"], d["T"]
+        prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, True, True)
+        o = torch.empty((B, H, T, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        ws = ba.workspace(ba.BAM_OP_FWD, B, H, T, dev)
+        ba.bam_attn_fwd(q, k, v, o, lse, prm, ws)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        (ka, kb_), = hook_events(torch, 1)
+        ms, kms = [], []
+        for _ in range(reps):
+            ba.bam_attn_profile_events(ba.BAM_KERNEL_FWD, ka, kb_)
+            a.record()
+            ba.bam_attn_fwd(q, k, v, o, lse, prm, ws)
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+            kms.append(ka.elapsed_time(kb_))
+        ba.bam_attn_profile_events(ba.BAM_KERNEL_FWD, None, None)
+        fl = pairs_causal(B, H, T) * 4 * D
+        tf = fl / (statistics.median(ms) * 1e-3) / 1e12
+        ktf = fl / (statistics.median(kms) * 1e-3) / 1e12
+        out[f"prefill_B{B}_H{H}_T{T}"] = {
+            "ms": round(statistics.median(ms), 4), "TFLOP/s": round(tf, 2),
+            "fwd_kernel_TFLOP/s": round(ktf, 2),
+            "frac_of_bf16_peak": round(ktf / peaks["bf16_tflops"], 4)}
+        del q, k, v, o, ws
+        torch.cuda.empty_cache()
+
+    d = make_inputs(5)
+    q, kc, vc = bf(d["q"]), bf(d["k"]), bf(d["v"])
+    p = {n: torch.from_numpy(d[n]).to(dev) for n in ("alpha", "beta", "mu", "s")}
+    B, H, Tkv = d["B"], d["H"], d["T"]
+    prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, True, True)
+    o = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = ba.workspace(ba.BAM_OP_DECODE, B, H, Tkv, dev)
+    ba.bam_attn_decode(q, kc, vc, o, lse, prm, ws)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    (ka, kb_), = hook_events(torch, 1)
+    ms, kms = [], []
+    for _ in range(max(5, steps // 2)):
+        ba.bam_attn_profile_events(ba.BAM_KERNEL_DECODE, ka, kb_)
+        a.record()
+        ba.bam_attn_decode(q, kc, vc, o, lse, prm, ws)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+        kms.append(ka.elapsed_time(kb_))
+    ba.bam_attn_profile_events(ba.BAM_KERNEL_DECODE, None, None)
+    kv_bytes = 2 * B * H * Tkv * D * 2
+    gbs = kv_bytes / (statistics.median(ms) * 1e-3) / 1e9
+    kgbs = kv_bytes / (statistics.median(kms) * 1e-3) / 1e9
+    out[f"decode_B{B}_H{H}_Tkv{Tkv}"] = {
+        "ms": round(statistics.median(ms), 4), "GB/s": round(gbs, 1),
+        "decode_kernel_GB/s": round(kgbs, 1), "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4)}
+    return out
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def oracle_sample_step(d, nbh, nthreads):
+    """fwd + bwd of the fp64 oracle on the first `nbh` (b, h) pairs of the
+    training workload; returns (seconds, flops)."""
+    import oracle
+    from transformer_attention_ggd_gb300.inputs import bf16_to_f64
+    B, H, T = d["B"], d["H"], d["T"]
+    bsel = max(1, nbh // H)
+    hsel = min(H, nbh)
+    sl = (slice(0, bsel), slice(0, hsel))
+    x = {n: bf16_to_f64(d[n][sl]) for n in ("q", "k", "v", "do")}
+    prm = {n: d[n][:hsel] for n in ("alpha", "beta", "mu", "s")}
+    t0 = time.perf_counter()
+    oracle.fwd(x["q"], x["k"], x["v"], prm["alpha"], prm["beta"], prm["mu"], prm["s"],
+               causal=True, ssmax=True, nthreads=nthreads)
+    oracle.bwd(x["q"], x["k"], x["v"], x["do"], prm["alpha"], prm["beta"], prm["mu"], prm["s"],
+               causal=True, ssmax=True, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, train_flops(bsel, hsel, T)
+
+
+def cpu_baseline(nbh=96):
+    from transformer_attention_ggd_gb300.inputs import make_inputs
+    import oracle
+    oracle.build()
+    d = make_inputs(2)
+    cores = os.cpu_count() or 1
+    dt, fl = oracle_sample_step(d, nbh, cores)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of {nbh} of the 96 (b,h) pairs of the B=8 H=12 "
+                      f"T=512 training step ({dt:.2f} s), scaled by algorithmic flops"}
+
+
+def run_reference(args):
+    from transformer_attention_ggd_gb300.inputs import make_inputs
+    import oracle
+    oracle.build()
+    d = make_inputs(2)
+    cores = os.cpu_count() or 1
+    nbh = 96
+    for _ in range(args.warmup):
+        oracle_sample_step(d, nbh, cores)
+    tot_t, tot_f = 0.0, 0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample_step(d, nbh, cores)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "train_B8_H12_T512", "B": 8, "H": 12, "T": 512, "D": D,
+                   "causal": True, "ssmax": True, "step": "fwd+bwd"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"each step: fp64 oracle fwd+bwd of {nbh} of the 96 (b,h) "
+                                   "pairs, scaled by algorithmic flops"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip prefill/decode extras")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    line, _ = run_ours(args, rank, world, dev, torch, dist)
+    if rank == 0:
+        peaks = load_peaks()
+        if not args.no_extra:
+            line["extra"] = extra_workloads(torch, dev, args.steps, peaks)
+        if not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
