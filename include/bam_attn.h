@@ -110,6 +110,29 @@ bam_status bam_attn_check_status(void* ws, cudaStream_t stream);
 /* Static description of a status code. */
 const char* bam_status_string(bam_status s);
 
+/* Decode without a workspace argument, for callers that cannot allocate
+ * device memory: plugin-style hosts that hand a library only its input and
+ * output pointers and own every other byte through their own allocator, or
+ * decode loops that cannot afford cudaMalloc's possible device-wide
+ * synchronisation.  The pages have no counterpart; this is an interface
+ * variant of bam_attn_decode (same kernels, same arguments and results).
+ *
+ * Scratch comes from a fixed array of BAM_DECODE_NOALLOC_SCRATCH_BYTES in
+ * the library's device image, held by every GPU that loads the library until
+ * the process exits.  Sizes whose scratch (the same amount that
+ * bam_attn_workspace_size(BAM_OP_DECODE, ...) reports) exceeds it return
+ * BAM_ERR_WORKSPACE before anything is launched.  Nothing is allocated or
+ * freed.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture on the device.  All calls share the array:
+ * calls that overlap on the GPU (for example on two streams) race on it.
+ * A device-side give-up of this path is recorded in that array and is not
+ * reported to the caller. */
+#define BAM_DECODE_NOALLOC_SCRATCH_BYTES (4u << 20)
+bam_status bam_attn_decode_noalloc(const void* q, const void* kc, const void* vc, void* o,
+                                   int o_fp32, float* lse, int B, int H, int Tkv, int D,
+                                   const bam_params* p, cudaStream_t stream);
+
 /* Kernels that bam_attn_profile_events can bracket. */
 enum {
   BAM_KERNEL_TABLE = 0,      /* distance-table kernel (fwd, bwd, decode)   */

@@ -47,7 +47,11 @@ EXPORTED = (
     "bam_status_string",
     "bam_attn_profile_events",
     "bam_attn_launch_count",
+    "bam_attn_decode_noalloc",
 )
+
+# Size of the fixed device scratch of bam_attn_decode_noalloc.
+BAM_DECODE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class BamError(RuntimeError):
@@ -101,6 +105,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bam_attn_profile_events.argtypes = [i, vp, vp]
         lib.bam_attn_launch_count.restype = ctypes.c_uint64
         lib.bam_attn_launch_count.argtypes = []
+        lib.bam_attn_decode_noalloc.restype = i
+        lib.bam_attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp]
         _lib = lib
         return lib
 
@@ -169,6 +175,20 @@ def bam_attn_decode(q, kc, vc, o, lse, params: BamParams, ws, stream=None) -> No
                                         B, H, Tkv, D, ctypes.byref(params), _ptr(ws), ws.numel(),
                                         _stream(stream))
     _check(st, "bam_attn_decode")
+
+
+def bam_attn_decode_noalloc(q, kc, vc, o, lse, params: BamParams, stream=None) -> None:
+    """Decode for callers that cannot allocate device memory (plugin-style
+    hosts that only pass input/output pointers; loops that cannot afford
+    cudaMalloc's possible synchronisation): no workspace argument, scratch
+    from the library's fixed device array.  Overlapping calls race."""
+    import torch
+    B, H, Tkv, D = kc.shape
+    o_fp32 = 1 if o.dtype == torch.float32 else 0
+    st = load_library().bam_attn_decode_noalloc(_ptr(q), _ptr(kc), _ptr(vc), _ptr(o), o_fp32,
+                                                _ptr(lse), B, H, Tkv, D, ctypes.byref(params),
+                                                _stream(stream))
+    _check(st, "bam_attn_decode_noalloc")
 
 
 def bam_attn_check_status(ws, stream=None) -> int:
