@@ -252,15 +252,18 @@ int bam_oracle_decode(const double* q, const double* kc, const double* vc, int B
 // grads: dalpha, dbeta, dmu, ds are [H] (summed over the batch).
 // absg (may be NULL): [4, H] sums of |per-element term| for each scalar gradient,
 // the scale against which a near-cancelling scalar gradient is judged.
+// absp (may be NULL): [4, H] sums of P_ij (|dP_ij| + |Delta_i|) |X_ij|, the
+// magnitudes before the cancellation inside dS = P (dP - Delta): the scale of
+// the rounding noise that any fp32 evaluation of the same sum carries.
 int bam_oracle_bwd(const double* q, const double* k, const double* v, const double* dO,
                    int B, int H, int T, int D, const double* alpha, const double* beta,
                    const double* mu, const double* s, double eps, int causal, int ssmax,
                    double* dq, double* dk, double* dv, double* dalpha, double* dbeta,
-                   double* dmu, double* ds, double* absg, int nthreads) {
+                   double* dmu, double* ds, double* absg, double* absp, int nthreads) {
     if (B < 1 || H < 1 || T < 1 || D < 1) return 1;
     Params p{alpha, beta, mu, s, eps, causal, ssmax};
     const int64_t BH = static_cast<int64_t>(B) * H;
-    std::vector<double> part(static_cast<size_t>(BH) * 8, 0.0);
+    std::vector<double> part(static_cast<size_t>(BH) * 12, 0.0);
     const double invsqrt = 1.0 / std::sqrt(static_cast<double>(D));
     parallel_for(BH, nthreads, [&](int64_t bh) {
         int h = static_cast<int>(bh % H);
@@ -276,7 +279,7 @@ int bam_oracle_bwd(const double* q, const double* k, const double* v, const doub
         std::fill(dkb, dkb + static_cast<size_t>(T) * D, 0.0);
         std::fill(dvb, dvb + static_cast<size_t>(T) * D, 0.0);
         std::vector<double> z(T), P(T), dP(T);
-        double acc[4] = {0, 0, 0, 0}, aabs[4] = {0, 0, 0, 0};
+        double acc[4] = {0, 0, 0, 0}, aabs[4] = {0, 0, 0, 0}, apre[4] = {0, 0, 0, 0};
         for (int i = 0; i < T; ++i) {
             int n = n_visible(i, T, causal);
             double c = row_scale(p, h, n, D);
@@ -316,15 +319,19 @@ int bam_oracle_bwd(const double* q, const double* k, const double* v, const doub
                 double gs = ssmax ? std::log(static_cast<double>(n)) * invsqrt * dot(qi, kj, D)
                                   : 0.0;
                 double t[4] = {dS * ga, dS * gbeta, dS * gm, dS * gs};
+                double x[4] = {ga, gbeta, gm, gs};
+                const double pre = P[j] * (std::fabs(dP[j]) + std::fabs(delta));
                 for (int w = 0; w < 4; ++w) {
                     acc[w] += t[w];
                     aabs[w] += std::fabs(t[w]);
+                    apre[w] += pre * std::fabs(x[w]);
                 }
             }
         }
         for (int w = 0; w < 4; ++w) {
-            part[static_cast<size_t>(bh) * 8 + w] = acc[w];
-            part[static_cast<size_t>(bh) * 8 + 4 + w] = aabs[w];
+            part[static_cast<size_t>(bh) * 12 + w] = acc[w];
+            part[static_cast<size_t>(bh) * 12 + 4 + w] = aabs[w];
+            part[static_cast<size_t>(bh) * 12 + 8 + w] = apre[w];
         }
     });
     double* outs[4] = {dalpha, dbeta, dmu, ds};
@@ -332,11 +339,14 @@ int bam_oracle_bwd(const double* q, const double* k, const double* v, const doub
         for (int h = 0; h < H; ++h) outs[w][h] = 0.0;
     if (absg)
         for (int w = 0; w < 4 * H; ++w) absg[w] = 0.0;
+    if (absp)
+        for (int w = 0; w < 4 * H; ++w) absp[w] = 0.0;
     for (int64_t bh = 0; bh < BH; ++bh) {
         int h = static_cast<int>(bh % H);
         for (int w = 0; w < 4; ++w) {
-            outs[w][h] += part[static_cast<size_t>(bh) * 8 + w];
-            if (absg) absg[w * H + h] += part[static_cast<size_t>(bh) * 8 + 4 + w];
+            outs[w][h] += part[static_cast<size_t>(bh) * 12 + w];
+            if (absg) absg[w * H + h] += part[static_cast<size_t>(bh) * 12 + 4 + w];
+            if (absp) absp[w * H + h] += part[static_cast<size_t>(bh) * 12 + 8 + w];
         }
     }
     return 0;

@@ -64,7 +64,7 @@ def _load():
                                               dp, dp, i]
             lib.bam_oracle_bwd.restype = i
             lib.bam_oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, dp, dp, dp, dp, d, i,
-                                           i, dp, dp, dp, dp, dp, dp, dp, dp, i]
+                                           i, dp, dp, dp, dp, dp, dp, dp, dp, dp, i]
             _lib = lib
     return _lib
 
@@ -151,8 +151,10 @@ def bwd(q, k, v, dO, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False
         nthreads=0):
     """Gradients of sum(O * dO).
 
-    Returns a dict with dq, dk, dv [B,H,T,D], dalpha, dbeta, dmu, ds [H] and
-    absg [4,H] (sum of |per-element term| of each scalar gradient).
+    Returns a dict with dq, dk, dv [B,H,T,D], dalpha, dbeta, dmu, ds [H],
+    absg [4,H] (sum of |per-element term| of each scalar gradient) and absp
+    [4,H] (sum of P (|dP| + |Delta|) |X|: the magnitudes before the
+    cancellation inside dS, which set the fp32 noise of any evaluation).
     """
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
     B, H, T, D = q.shape
@@ -160,11 +162,13 @@ def bwd(q, k, v, dO, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False
     dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
     g = [np.empty(H, dtype=np.float64) for _ in range(4)]
     absg = np.empty((4, H), dtype=np.float64)
+    absp = np.empty((4, H), dtype=np.float64)
     rc = _load().bam_oracle_bwd(_dp(q), _dp(k), _dp(v), _dp(dO), B, H, T, D, _dp(a), _dp(b),
                                 _dp(m), _dp(sc), float(eps), int(bool(causal)),
                                 int(bool(ssmax)), _dp(dq), _dp(dk), _dp(dv), _dp(g[0]),
-                                _dp(g[1]), _dp(g[2]), _dp(g[3]), _dp(absg), int(nthreads))
+                                _dp(g[1]), _dp(g[2]), _dp(g[3]), _dp(absg), _dp(absp),
+                                int(nthreads))
     if rc != 0:
         raise ValueError("oracle bwd: bad sizes")
     return {"dq": dq, "dk": dk, "dv": dv, "dalpha": g[0], "dbeta": g[1], "dmu": g[2],
-            "ds": g[3], "absg": absg}
+            "ds": g[3], "absg": absg, "absp": absp}

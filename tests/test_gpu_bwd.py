@@ -49,7 +49,7 @@ def _compare(got, ref, ssmax):
         if n == "ds" and not ssmax:
             assert np.all(got[n] == 0.0)
             continue
-        err = scalar_rel_err(got[n], ref[n], ref["absg"][w])
+        err = scalar_rel_err(got[n], ref[n], ref["absg"][w], ref["absp"][w])
         assert err.max() <= GRAD_RTOL, f"{n}: {got[n]} vs {ref[n]} (err {err.max():.3e})"
 
 

@@ -320,9 +320,11 @@ def test_gradients_match_finite_differences(causal, ssmax, T, mu0, beta):
         assert np.all(g["ds"] == 0.0)
     # Invariant: softmax weights sum to one, so sum_j dv_j = sum_i dO_i.
     np.testing.assert_allclose(g["dv"].sum(axis=2), dO.sum(axis=2), rtol=1e-12, atol=1e-12)
-    # absg bounds each scalar gradient.
+    # absg bounds each scalar gradient, and absp bounds absg
+    # (|dS X| = P |dP - Delta| |X| <= P (|dP| + |Delta|) |X|).
     for w, name in enumerate(("dalpha", "dbeta", "dmu", "ds")):
         assert np.all(np.abs(g[name]) <= g["absg"][w] * (1 + 1e-12) + 1e-300)
+        assert np.all(g["absg"][w] <= g["absp"][w] * (1 + 1e-12) + 1e-300)
 
 
 def test_bias_grad_matches_finite_differences():
