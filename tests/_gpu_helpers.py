@@ -8,18 +8,18 @@ from transformer_attention_ggd_gb300.inputs import bf16_bits, bf16_to_f64
 # Tolerances: O is compared in fp32 output mode with a max-abs bound of 1e-2;
 # gradients (dq, dk, dv) and the per-head scalar gradients with a relative
 # bound of 2e-2.  "Relative" for a tensor: max|g - g*| / max(max|g*|, 1e-3);
-# for a scalar: |g - g*| / max(|g*|, 1e-2 * sum|dS X|, 1e-5 * sum P(|dP|+|Delta|)|X|).
+# for a scalar: |g - g*| / max(|g*|, 1e-2 * sum|dS X|, 1e-4 * sum P(|dP|+|Delta|)|X|).
 # The last two terms only matter where the reference cancels: dS = P(dP -
-# Delta) is a difference, and any fp32 evaluation of it carries noise of
-# order 1e-7 of |dP| + |Delta|, which a large table value X (for example
-# db/dbeta of an eps-clamped head) multiplies; a row with a single key has
-# dS = 0 exactly.  1e-5 of the pre-cancellation magnitude is ~100x the fp32
-# unit roundoff.  The tensor floor likewise keeps an all-zero reference (T = 1)
-# from dividing fp32 noise by zero.
+# Delta) is a difference, and an fp32 evaluation with hardware exp2 (relative
+# error ~2^-22) carries noise of a few 1e-7 of P(|dP| + |Delta|), which a large
+# table value X (db/dbeta of an eps-clamped head) multiplies; a row with a
+# single key has dS = 0 exactly.  With the 2e-2 factor the floor is 2e-6 of
+# the pre-cancellation magnitude.  The tensor floor likewise keeps an
+# all-zero reference (T = 1) from dividing fp32 noise by zero.
 O_ATOL = 1e-2
 GRAD_RTOL = 2e-2
 GRAD_FLOOR = 1e-3
-SCALAR_NOISE = 1e-5
+SCALAR_NOISE = 1e-4
 # LSE is not bounded by the method's stated tolerances.  Logits are fp32 dot
 # products of bf16 inputs plus an fp32 table value, so LSE carries the fp32
 # representation error of the logit itself (relative ~6e-8; an eps-clamped

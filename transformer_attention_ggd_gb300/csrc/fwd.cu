@@ -277,23 +277,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&sm.k_full[s], (j / kStages) & 1, a.status, ab, kSiteSoftK);
       if (!ok) break;
       tc_fence_after();
-      // S row -> z = c_i S + bias (log2 units), 32 columns at a time; the
-      // next chunk's TMEM load overlaps this chunk's arithmetic.
+      // S row -> z = c_i S + bias (log2 units) as column pairs (f32x2), 32
+      // columns at a time; the next chunk's TMEM load overlaps this chunk's
+      // arithmetic.
       const float* wv = sm.win[s] + woff;
-      float z[128];
-      uint32_t sr[2][32];
-      tmem_ld_32x32b_x32(tS, sr[0]);
+      const uint64_t cr2 = f2_pack(cr, cr);
+      uint64_t z[64];
+      uint32_t sr[2][16];
+      tmem_ld_32x32b_x16(tS, sr[0]);
       tmem_ld_wait();
-      reg_fence32(sr[0]);
+      reg_fence16(sr[0]);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        if (ch < 3) tmem_ld_32x32b_x32(tS + 32 * (ch + 1), sr[(ch + 1) & 1]);
+      for (int ch = 0; ch < 8; ++ch) {
+        if (ch < 7) tmem_ld_32x32b_x16(tS + 16 * (ch + 1), sr[(ch + 1) & 1]);
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          z[32 * ch + c] = fmaf(__uint_as_float(sr[ch & 1][c]), cr, wv[-(32 * ch + c)]);
-        if (ch < 3) {
+        for (int x = 0; x < 8; ++x) {
+          const int c = 16 * ch + 2 * x;
+          const uint64_t s2 = f2_pack(__uint_as_float(sr[ch & 1][2 * x]),
+                                      __uint_as_float(sr[ch & 1][2 * x + 1]));
+          z[8 * ch + x] = ffma2(s2, cr2, f2_pack(wv[-c], wv[-c - 1]));
+        }
+        if (ch < 7) {
           tmem_ld_wait();
-          reg_fence32(sr[(ch + 1) & 1]);
+          reg_fence16(sr[(ch + 1) & 1]);
         }
       }
       tc_fence_before();
@@ -307,12 +313,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         int lim = a.T - 1 - j0;
         if (a.causal) lim = min(lim, i - j0);
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > lim) z[c] = -INFINITY;
+        for (int x = 0; x < 64; ++x) {
+          float lo, hi;
+          f2_unpack(z[x], lo, hi);
+          if (2 * x > lim) lo = -INFINITY;
+          if (2 * x + 1 > lim) hi = -INFINITY;
+          z[x] = f2_pack(lo, hi);
+        }
       }
-      float mx = z[0];
+      // Row max: four independent chains of 3-input max.
+      float mq[4];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, z[c]);
+      for (int x = 0; x < 4; ++x) {
+        float lo, hi;
+        f2_unpack(z[x], lo, hi);
+        mq[x] = fmaxf(lo, hi);
+      }
+#pragma unroll
+      for (int x = 4; x < 64; ++x) {
+        float lo, hi;
+        f2_unpack(z[x], lo, hi);
+        mq[x & 3] = fmax3(mq[x & 3], lo, hi);
+      }
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float m_new = fmaxf(m, mx);
       const bool resc = m_new > m + kRescaleThreshold;
       float scale = 1.0f;
@@ -322,27 +345,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         le *= scale;
         m = m_new;
       }
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(z[2 * c] - m);
-        const float p1 = ex2_approx(z[2 * c + 1] - m);
-        const uint32_t w = pack_bf16x2(p0, p1);
-        pk[c] = w;
-        // O is normalised by the sum of the bf16-rounded weights that the PV
-        // product uses (an exact weighted average of V under those weights);
-        // the LSE keeps the sum of the unrounded weights.
-        l += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
-        le += p0 + p1;
-      }
       if (j > 0) {
         // PV of the previous tile must be done: frees P and makes O stable.
         ok = warp_wait(&sm.pv_done[t], (j - 1) & 1, a.status, ab, kSiteSoftPV);
         if (!ok) break;
         tc_fence_after();
       }
-      tmem_st_32x32b_x32(tP, pk);
-      tmem_st_32x32b_x32(tP + 32, pk + 32);
+      // Probabilities as bf16 pairs for the PV product, streamed to TMEM 32
+      // columns at a time, and the two row sums (rounded weights for O,
+      // unrounded for the LSE) in independent partial sums.
+      const uint64_t negm2 = f2_pack(-m, -m);
+      uint64_t lr2[2] = {0ull, 0ull}, le2[2] = {0ull, 0ull};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int y = 0; y < 16; ++y) {
+          const int x = 16 * q + y;
+          float a0, a1;
+          f2_unpack(fadd2(z[x], negm2), a0, a1);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          const uint32_t w = pack_bf16x2(p0, p1);
+          pk[y] = w;
+          lr2[y & 1] = fadd2(lr2[y & 1], f2_pack(__uint_as_float(w << 16),
+                                                 __uint_as_float(w & 0xFFFF0000u)));
+          le2[y & 1] = fadd2(le2[y & 1], f2_pack(p0, p1));
+        }
+        tmem_st_32x32b_x16(tP + 16 * q, pk);
+      }
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(fadd2(lr2[0], lr2[1]), a0, a1);
+        f2_unpack(fadd2(le2[0], le2[1]), b0, b1);
+        l += a0 + a1;
+        le += b0 + b1;
+      }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         uint32_t ov[64];
         tmem_ld_32x32b_x32(tO, ov);
