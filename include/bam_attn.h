@@ -135,9 +135,9 @@ bam_status bam_attn_decode_noalloc(const void* q, const void* kc, const void* vc
 
 /* Kernels that bam_attn_profile_events can bracket. */
 enum {
-  BAM_KERNEL_TABLE = 0,      /* distance-table kernel (fwd, bwd, decode)   */
+  BAM_KERNEL_TABLE = 0,      /* distance-table kernel (fwd, decode)        */
   BAM_KERNEL_FWD = 1,        /* fused forward                               */
-  BAM_KERNEL_BWD_PREP = 2,   /* backward preprocess (Delta, zeroing)        */
+  BAM_KERNEL_BWD_PREP = 2,   /* backward preprocess (tables, Delta, zeroing) */
   BAM_KERNEL_BWD = 3,        /* fused backward                              */
   BAM_KERNEL_BWD_FINAL = 4,  /* dq conversion and scalar-gradient finish    */
   BAM_KERNEL_DECODE = 5,     /* split-KV decode                             */

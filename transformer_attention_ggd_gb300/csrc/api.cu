@@ -289,12 +289,9 @@ bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void*
   float* table = reinterpret_cast<float*>(wsb + w.table);
   const TableGeom g = table_geom(T, p->causal);
 
-  TableArgs ta{table, p->alpha, p->beta, p->mu, status, p->eps, H, g.len, g.off, 0,
-               kTableBackward};
-  cudaError_t e = launch_kernel(BAM_KERNEL_TABLE, stream, [&] { return launch_table(ta, stream); });
-  if (e != cudaSuccess) return BAM_ERR_CUDA;
-
   BwdArgs ba;
+  ba.tab = TableArgs{table, p->alpha, p->beta, p->mu, status, p->eps, H, g.len, g.off, 0,
+                     kTableBackward};
   ba.o = o;
   ba.dO = static_cast<const uint16_t*>(dO);
   ba.lse = lse;
@@ -324,7 +321,8 @@ bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void*
   ba.o_fp32 = o_fp32 ? 1 : 0;
   ba.tab_len = g.len;
   ba.tab_off = g.off;
-  e = launch_kernel(BAM_KERNEL_BWD_PREP, stream, [&] { return launch_bwd_prep(ba, stream); });
+  cudaError_t e =
+      launch_kernel(BAM_KERNEL_BWD_PREP, stream, [&] { return launch_bwd_prep(ba, stream); });
   if (e != cudaSuccess) return BAM_ERR_CUDA;
   e = launch_kernel(BAM_KERNEL_BWD, stream,
                     [&] { return launch_bwd(tq, tk, tv, tdo, ba, stream); });

@@ -106,7 +106,36 @@ struct BwdArgs {
   int B, H, T, nkb;
   int causal, ssmax, o_fp32;
   int tab_len, tab_off;
+  TableArgs tab;        // the three distance tables, built by the preprocess
 };
+
+// Launch with an optional programmatic-dependent-launch attribute: the
+// kernel may start while the previous kernel on the stream finishes, and must
+// execute griddepcontrol.wait before touching anything that kernel writes.
+// Only the second and later kernels of one entry point use it, so that two
+// calls sharing a workspace never overlap.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // Internal launchers (one per kernel).  Each returns the launch error.
 cudaError_t launch_table(const TableArgs& a, cudaStream_t st);

@@ -18,24 +18,27 @@
 //
 // One CTA owns a 128-key tile of one (b, h) and walks the 128-row query
 // tiles that see it:
-//   warp 4     TMA producer: K, V once; per query tile Q, dO and the three
+//   warp 8     TMA producer: K, V once; per query tile Q, dO and the three
 //              256-entry distance windows (b, db/dbeta, db/dmu), 2 stages.
-//   warp 5     MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
+//   warp 9     MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
 //              dV += P^T dO and dK += (c dS)^T Q (A operands MN-major in shared
 //              memory, M = keys) and dQ = (c dS) K (A = c dS from TMEM).
-//   warps 0-3  one thread per query row: P, dS, the four scalar-gradient
-//              sums, P and c*dS to shared memory and c*dS to TMEM, then the
-//              dQ tile added to an fp32 accumulator with vector reductions.
-//              At the end, dK and dV rows (TMEM lane = key) go out as bf16.
+//   warps 0-7  two warps per TMEM lane quarter; each thread owns one query
+//              row and one half (64 keys) of the tile: P, dS, the scalar-
+//              gradient sums (as f32x2 pairs of partial sums), P and c*dS to
+//              shared memory and c*dS to TMEM, then its half of the dQ tile
+//              added to an fp32 accumulator with vector reductions.  At the
+//              end, dK and dV rows (TMEM lane = key) go out as bf16.
 // TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
 //               dK [384,448) dV [448,512).
-#include "bam_common.cuh"
+#include "table_eval.cuh"
 
 namespace bam {
 namespace {
 
 constexpr int kBStages = 2;
-constexpr int kBThreads = 192;
+constexpr int kBThreads = 320;   // 8 element-wise warps, producer, MMA issuer
+constexpr int kBCompute = 8;
 constexpr int kTile = 128 * 64 * 2;  // 16 KB bf16 tile
 constexpr int kBWin = 256;
 
@@ -47,7 +50,7 @@ struct __align__(1024) BwdSmem {
   uint8_t pt[2 * kTile];   // P^T as an MN-major A operand: 2 atoms of 64 keys x 128 queries
   uint8_t dst[2 * kTile];  // (c dS)^T, same layout
   float win[kBStages][3][kBWin];
-  float red[4][4];
+  float red[kBCompute][4];
   uint64_t kv_full;
   uint64_t qd_full[kBStages];
   uint64_t qd_empty[kBStages];
@@ -113,6 +116,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
+    // Tables, Delta and the zeroed accumulators come from the preprocess.
+    grid_dep_wait();
     sm.abort_flag = *reinterpret_cast<volatile int*>(&a.status->abort);
     mbar_init(&sm.kv_full, 1);
     for (int s = 0; s < kBStages; ++s) {
@@ -120,12 +125,12 @@ __global__ void __launch_bounds__(kBThreads, 1)
       mbar_init(&sm.qd_empty[s], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.ds_ready, 4);
+    mbar_init(&sm.ds_ready, kBCompute);
     mbar_init(&sm.mma_done, 1);
     mbar_init(&sm.mma_final, 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   const uint32_t tm = sm.tmem_base;
   const size_t plane = static_cast<size_t>(a.H) * a.tab_len;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = (*ab == 0);
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       for (int t = max(0, issued - kBStages); t < issued; ++t)
         mbar_drain(&sm.qd_full[t % kBStages], (t / kBStages) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = (*ab == 0);
@@ -230,23 +235,26 @@ __global__ void __launch_bounds__(kBThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ element-wise
-    const int r = threadIdx.x;  // query row within the tile = TMEM lane
+    const int r = 32 * (warp & 3) + lane;  // query row within the tile = TMEM lane
+    const int hc = warp >> 2;              // which 64 keys of the tile
     const uint32_t lb = tmem_lane_base(warp);
     const float s_h = a.ssmax ? __ldg(a.s + h) : 1.0f;
-    float acc_b = 0.f, acc_beta = 0.f, acc_mu = 0.f, acc_s = 0.f;
+    // Scalar-gradient sums as f32x2 pairs (even / odd key columns):
+    // sum dS b (log2 units), sum dS db/dbeta, sum dS db/dmu, and sum over
+    // rows of w_i * sum_j dS S.
+    uint64_t accB2 = 0ull, accBeta2 = 0ull, accMu2 = 0ull;
+    float acc_s = 0.f;
     bool ok = (*ab == 0);
     auto dq_epilogue = [&](int t) {
       const int i = (q_first + t) * 128 + r;
-      uint32_t dv[64];
-      tmem_ld_32x32b_x32(tm + lb + kColDQ, dv);
-      tmem_ld_32x32b_x32(tm + lb + kColDQ + 32, dv + 32);
+      uint32_t dv[32];
+      tmem_ld_32x32b_x32(tm + lb + kColDQ + 32 * hc, dv);
       tmem_ld_wait();
       reg_fence32(dv);
-      reg_fence32(dv + 32);
       if (i < a.T) {
-        float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.T + i) * kHeadDim;
+        float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.T + i) * kHeadDim + 32 * hc;
 #pragma unroll
-        for (int x = 0; x < 16; ++x)
+        for (int x = 0; x < 8; ++x)
           red_add_v4(dst + 4 * x, __uint_as_float(dv[4 * x]), __uint_as_float(dv[4 * x + 1]),
                      __uint_as_float(dv[4 * x + 2]), __uint_as_float(dv[4 * x + 3]));
       }
@@ -267,6 +275,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
       int lim = a.T - 1 - j0;              // last visible key column
       if (a.causal) lim = min(lim, i - j0);
       const bool need_mask = lim < 127;
+      const uint64_t cr2 = f2_pack(cr, cr), cn2 = f2_pack(cn, cn);
+      const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndel2 = f2_pack(-delta, -delta);
 
       ok = warp_wait(&sm.s_full, t & 1, a.status, ab, kSiteBWgS);
       if (!ok) break;
@@ -284,63 +294,77 @@ __global__ void __launch_bounds__(kBThreads, 1)
       const float* wb = sm.win[s][0] + 128 + r;
       const float* wbeta = sm.win[s][1] + 128 + r;
       const float* wmu = sm.win[s][2] + 128 + r;
-      float row_ss = 0.f;
-      float pb = 0.f, pbeta = 0.f, pmu = 0.f, ps = 0.f, pdp = 0.f;  // sum_j P X, sum_j P dP
+      // Row partial sums for the Delta correction and the SSMax sum.
+      uint64_t pB2 = 0ull, pBeta2 = 0ull, pMu2 = 0ull, pS2 = 0ull, pDP2 = 0ull, rowSS2 = 0ull;
+      uint32_t pp[16], dd[16];
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
+        const int c0 = 64 * hc + 32 * ch;
         uint32_t sv[32], dpv[32];
-        tmem_ld_32x32b_x32(tm + lb + kColS + 32 * ch, sv);
-        tmem_ld_32x32b_x32(tm + lb + kColDP + 32 * ch, dpv);
+        tmem_ld_32x32b_x32(tm + lb + kColS + c0, sv);
+        tmem_ld_32x32b_x32(tm + lb + kColDP + c0, dpv);
         tmem_ld_wait();
         reg_fence32(sv);
         reg_fence32(dpv);
-        uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 32 * ch + x + e;
-            const float sval = __uint_as_float(sv[x + e]);
-            const float tb = wb[-c];
-            float zz = fmaf(sval, cr, tb);
-            if (need_mask && c > lim) zz = -INFINITY;
-            const float p = ex2_approx(zz - lse2);
-            const float dpval = __uint_as_float(dpv[x + e]);
-            const float dS = p * (dpval - delta);
-            const float tbeta = wbeta[-c], tmu = wmu[-c];
-            acc_b = fmaf(dS, tb, acc_b);
-            acc_beta = fmaf(dS, tbeta, acc_beta);
-            acc_mu = fmaf(dS, tmu, acc_mu);
-            row_ss = fmaf(dS, sval, row_ss);
-            pb = fmaf(p, tb, pb);
-            pbeta = fmaf(p, tbeta, pbeta);
-            pmu = fmaf(p, tmu, pmu);
-            ps = fmaf(p, sval, ps);
-            pdp = fmaf(p, dpval, pdp);
-            pv[e] = p;
-            dsv[e] = dS * cn;
+        for (int x = 0; x < 16; ++x) {
+          const int c = c0 + 2 * x;
+          const uint64_t s2 = f2_pack(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
+          const uint64_t dp2 =
+              f2_pack(__uint_as_float(dpv[2 * x]), __uint_as_float(dpv[2 * x + 1]));
+          const uint64_t tb2 = f2_pack(wb[-c], wb[-c - 1]);
+          const uint64_t tbeta2 = f2_pack(wbeta[-c], wbeta[-c - 1]);
+          const uint64_t tmu2 = f2_pack(wmu[-c], wmu[-c - 1]);
+          float z0, z1;
+          f2_unpack(fadd2(ffma2(s2, cr2, tb2), nlse2), z0, z1);
+          if (need_mask) {
+            if (c > lim) z0 = -INFINITY;
+            if (c + 1 > lim) z1 = -INFINITY;
           }
-          pp[x / 2] = pack_bf16x2(pv[0], pv[1]);
-          dd[x / 2] = pack_bf16x2(dsv[0], dsv[1]);
+          const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+          const uint64_t p2 = f2_pack(p0, p1);
+          const uint64_t dS2 = fmul2(p2, fadd2(dp2, ndel2));
+          accB2 = ffma2(dS2, tb2, accB2);
+          accBeta2 = ffma2(dS2, tbeta2, accBeta2);
+          accMu2 = ffma2(dS2, tmu2, accMu2);
+          rowSS2 = ffma2(dS2, s2, rowSS2);
+          pB2 = ffma2(p2, tb2, pB2);
+          pBeta2 = ffma2(p2, tbeta2, pBeta2);
+          pMu2 = ffma2(p2, tmu2, pMu2);
+          pS2 = ffma2(p2, s2, pS2);
+          pDP2 = ffma2(p2, dp2, pDP2);
+          pp[x] = pack_bf16x2(p0, p1);
+          float q0, q1;
+          f2_unpack(fmul2(dS2, cn2), q0, q1);
+          dd[x] = pack_bf16x2(q0, q1);
         }
-        // P and c*dS, keys [32ch, 32ch+32) of query row r, into the MN-major
+        // P and c*dS, keys [c0, c0+32) of query row r, into the MN-major
         // operands (four 16-byte chunks each) and c*dS into TMEM.
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
-          const uint32_t off = mn_chunk_offset(4 * ch + q8, r);
+          const uint32_t off = mn_chunk_offset(c0 / 8 + q8, r);
           *reinterpret_cast<uint4*>(sm.pt + off) =
               make_uint4(pp[4 * q8], pp[4 * q8 + 1], pp[4 * q8 + 2], pp[4 * q8 + 3]);
           *reinterpret_cast<uint4*>(sm.dst + off) =
               make_uint4(dd[4 * q8], dd[4 * q8 + 1], dd[4 * q8 + 2], dd[4 * q8 + 3]);
         }
-        tmem_st_32x32b_x16(tm + lb + kColDS + 16 * ch, dd);
+        tmem_st_32x32b_x16(tm + lb + kColDS + c0 / 2, dd);
       }
-      acc_s = fmaf(row_ss, w_ln, acc_s);
+      {
+        float a0, a1;
+        f2_unpack(rowSS2, a0, a1);
+        acc_s = fmaf(a0 + a1, w_ln, acc_s);
+      }
       if (row_ok) {
+        float b0, b1, e0, e1, m0, m1, s0, s1, d0, d1;
+        f2_unpack(pB2, b0, b1);
+        f2_unpack(pBeta2, e0, e1);
+        f2_unpack(pMu2, m0, m1);
+        f2_unpack(pS2, s0, s1);
+        f2_unpack(pDP2, d0, d1);
         float* ra = a.rowacc + ridx * 8;
-        red_add_v4(ra, pb, pbeta, pmu, ps * w_ln);
-        red_add_v4(ra + 4, pdp, 0.f, 0.f, 0.f);
+        red_add_v4(ra, b0 + b1, e0 + e1, m0 + m1, (s0 + s1) * w_ln);
+        atomicAdd(ra + 4, d0 + d1);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -353,21 +377,21 @@ __global__ void __launch_bounds__(kBThreads, 1)
       if (ok) {
         tc_fence_after();
         dq_epilogue(nq - 1);
-        // dK and dV rows: TMEM lane = key j0 + r.
+        // dK and dV rows: TMEM lane = key j0 + r; this warp writes 32 of the
+        // 64 dimensions.
         const int j = j0 + r;
-        uint32_t kvv[64];
         for (int which = 0; which < 2; ++which) {
-          const uint32_t col = which ? kColDV : kColDK;
+          const uint32_t col = (which ? kColDV : kColDK) + 32 * hc;
+          uint32_t kvv[32];
           tmem_ld_32x32b_x32(tm + lb + col, kvv);
-          tmem_ld_32x32b_x32(tm + lb + col + 32, kvv + 32);
           tmem_ld_wait();
           reg_fence32(kvv);
-          reg_fence32(kvv + 32);
           if (j < a.T) {
-            uint16_t* out = (which ? a.dv : a.dk) + (static_cast<size_t>(bh) * a.T + j) * kHeadDim;
+            uint16_t* out =
+                (which ? a.dv : a.dk) + (static_cast<size_t>(bh) * a.T + j) * kHeadDim + 32 * hc;
             uint4* o4 = reinterpret_cast<uint4*>(out);
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
+            for (int x = 0; x < 4; ++x)
               o4[x] = make_uint4(
                   pack_bf16x2(__uint_as_float(kvv[8 * x]), __uint_as_float(kvv[8 * x + 1])),
                   pack_bf16x2(__uint_as_float(kvv[8 * x + 2]), __uint_as_float(kvv[8 * x + 3])),
@@ -377,47 +401,56 @@ __global__ void __launch_bounds__(kBThreads, 1)
         }
       }
     }
-    // Causal key tiles beyond every query contribute nothing; write their dK, dV.
-    if (ok && nq == 0) {
-      const int j = j0 + r;
-      if (j < a.T) {
-        uint4* k4 = reinterpret_cast<uint4*>(a.dk + (static_cast<size_t>(bh) * a.T + j) * kHeadDim);
-        uint4* v4 = reinterpret_cast<uint4*>(a.dv + (static_cast<size_t>(bh) * a.T + j) * kHeadDim);
-        for (int x = 0; x < 8; ++x) {
-          k4[x] = make_uint4(0, 0, 0, 0);
-          v4[x] = make_uint4(0, 0, 0, 0);
-        }
-      }
-    }
     // Block reduction of the scalar-gradient sums, one atomic per head and sum.
-    float v4[4] = {acc_b, acc_beta, acc_mu, acc_s};
+    float v4[4];
+    {
+      float a0, a1;
+      f2_unpack(accB2, a0, a1);
+      v4[0] = a0 + a1;
+      f2_unpack(accBeta2, a0, a1);
+      v4[1] = a0 + a1;
+      f2_unpack(accMu2, a0, a1);
+      v4[2] = a0 + a1;
+      v4[3] = acc_s;
+    }
 #pragma unroll
     for (int x = 0; x < 4; ++x)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v4[x] += __shfl_xor_sync(0xffffffffu, v4[x], off);
     if (lane == 0)
       for (int x = 0; x < 4; ++x) sm.red[warp][x] = v4[x];
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kBCompute) : "memory");
     if (threadIdx.x < 4 && ok) {
-      const float tot = sm.red[0][threadIdx.x] + sm.red[1][threadIdx.x] +
-                        sm.red[2][threadIdx.x] + sm.red[3][threadIdx.x];
+      float tot = 0.f;
+      for (int w = 0; w < kBCompute; ++w) tot += sm.red[w][threadIdx.x];
       atomicAdd(a.gacc + threadIdx.x * a.H + h, tot);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  grid_dep_trigger();
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tm, 512);
   }
 }
 
-// Delta_i = dO_i . O_i; zero the dq accumulator and the scalar sums.
-__global__ void bam_bwd_prep_kernel(const BwdArgs a) {
+// The three distance tables (first `table_blocks` blocks); Delta_i = dO_i .
+// O_i; zero the dq accumulator, the row sums and the scalar sums.
+__global__ void __launch_bounds__(256) bam_bwd_prep_kernel(const BwdArgs a, int table_blocks) {
+  grid_dep_trigger();
+  if (static_cast<int>(blockIdx.x) < table_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x < 4) reinterpret_cast<int*>(a.status)[threadIdx.x] = 0;
+    const size_t n = static_cast<size_t>(a.tab.H) * a.tab.len;
+    for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
+         e += static_cast<size_t>(table_blocks) * blockDim.x)
+      table_entry(a.tab, static_cast<int>(e / a.tab.len), static_cast<int>(e % a.tab.len));
+    return;
+  }
   const size_t rows = static_cast<size_t>(a.B) * a.H * a.T;
-  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const size_t tid = static_cast<size_t>(blockIdx.x - table_blocks) * blockDim.x + threadIdx.x;
+  const size_t nthreads = static_cast<size_t>(gridDim.x - table_blocks) * blockDim.x;
   for (size_t row = tid; row < rows; row += nthreads) {
     const uint4* g = reinterpret_cast<const uint4*>(a.dO + row * kHeadDim);
     float acc = 0.f;
@@ -464,6 +497,7 @@ __global__ void bam_bwd_prep_kernel(const BwdArgs a) {
 constexpr int kFinalRows = 2048;
 
 __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
+  grid_dep_wait();  // dq accumulator, row sums and scalar sums of the fused kernel
   const size_t n8 = static_cast<size_t>(a.B) * a.H * a.T * (kHeadDim / 8);
   const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -529,10 +563,15 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
 
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st) {
   const size_t rows = static_cast<size_t>(a.B) * a.H * a.T;
-  const size_t want = (rows * 16 + 255) / 256;
-  const unsigned grid = static_cast<unsigned>(want < 152 * 8 ? (want < 1 ? 1 : want) : 152 * 8);
-  bam_bwd_prep_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  size_t want = (rows * 16 + 255) / 256;
+  if (want < 1) want = 1;
+  if (want > 152 * 8) want = 152 * 8;
+  const size_t tab_entries = static_cast<size_t>(a.tab.H) * a.tab.len;
+  size_t tb = (tab_entries + 255) / 256;
+  if (tb > 152 * 2) tb = 152 * 2;
+  const unsigned grid = static_cast<unsigned>(want + tb);
+  return launch_k(bam_bwd_prep_kernel, dim3(grid), dim3(256), 0, st, false, a,
+                  static_cast<int>(tb));
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -547,8 +586,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     attr_set = true;
   }
   const unsigned grid = static_cast<unsigned>(a.nkb) * static_cast<unsigned>(a.B * a.H);
-  bam_bwd_kernel<<<grid, kBThreads, smem, st>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError();
+  return launch_k(bam_bwd_kernel, dim3(grid), dim3(kBThreads), smem, st, true, tq, tk, tv, tdo,
+                  a);
 }
 
 cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
@@ -558,8 +597,7 @@ cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
   if (want < items) want = items;
   if (want > 152 * 8) want = 152 * 8;
   const unsigned grid = static_cast<unsigned>(want);
-  bam_bwd_final_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(bam_bwd_final_kernel, dim3(grid), dim3(256), 0, st, true, a);
 }
 
 }  // namespace bam

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kDecThreads)
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
+    grid_dep_wait();  // the decode table comes from the previous kernel
     sm.abort_flag = *reinterpret_cast<volatile int*>(&a.status->abort);
     for (int s = 0; s < kDecStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(kDecThreads)
     }
   }
   __syncthreads();
+  grid_dep_trigger();
   // Merge the four consumer warps and write this chunk's partial.
   if (threadIdx.x < kHeadDim && *ab == 0) {
     const int x = threadIdx.x;
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(kDecThreads)
 
 // One warp per (b, h): merge the split partials, normalise, write O and LSE.
 __global__ void __launch_bounds__(128) bam_decode_combine_kernel(const DecodeArgs a) {
+  grid_dep_wait();  // partials of the decode kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x * 4 + warp;
   if (bh >= a.B * a.H) return;
@@ -273,14 +276,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     attr_set = true;
   }
   dim3 grid(a.nsplit, a.B * a.H);
-  bam_decode_kernel<<<grid, kDecThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(bam_decode_kernel, grid, dim3(kDecThreads), smem, st, true, a);
 }
 
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t st) {
   const int BH = a.B * a.H;
-  bam_decode_combine_kernel<<<(BH + 3) / 4, 128, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_k(bam_decode_combine_kernel, dim3((BH + 3) / 4), dim3(128), 0, st, true, a);
 }
 
 }  // namespace bam

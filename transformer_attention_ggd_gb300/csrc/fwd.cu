@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
+    // The distance table (and the cleared status word) come from the
+    // previous kernel of this call.
+    grid_dep_wait();
     sm.abort_flag = *reinterpret_cast<volatile int*>(&a.status->abort);
     mbar_init(&sm.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -439,8 +442,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     attr_set = true;
   }
   const unsigned grid = static_cast<unsigned>(a.nqb) * static_cast<unsigned>(a.B * a.H);
-  bam_fwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  return launch_k(bam_fwd_kernel, dim3(grid), dim3(kThreads), smem, st, true, tq, tk, tv, a);
 }
 
 }  // namespace bam
