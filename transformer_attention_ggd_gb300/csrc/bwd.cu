@@ -18,17 +18,17 @@
 //
 // One CTA owns a 128-key tile of one (b, h) and walks the 128-row query
 // tiles that see it:
-//   warp 8     TMA producer: K, V once; per query tile Q, dO and the three
+//   warp 16    TMA producer: K, V once; per query tile Q, dO and the three
 //              256-entry distance windows (b, db/dbeta, db/dmu), 2 stages.
-//   warp 9     MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
+//   warp 17    MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
 //              dV += P^T dO and dK += (c dS)^T Q (A operands MN-major in shared
 //              memory, M = keys) and dQ = (c dS) K (A = c dS from TMEM).
-//   warps 0-7  two warps per TMEM lane quarter; each thread owns one query
-//              row and one half (64 keys) of the tile: P, dS, the scalar-
+//   warps 0-15 four warps per TMEM lane quarter; each thread owns one query
+//              row and one quarter (32 keys) of the tile: P, dS, the scalar-
 //              gradient sums (as f32x2 pairs of partial sums), P and c*dS to
-//              shared memory and c*dS to TMEM, then its half of the dQ tile
-//              added to an fp32 accumulator with vector reductions.  At the
-//              end, dK and dV rows (TMEM lane = key) go out as bf16.
+//              shared memory and c*dS to TMEM, then its quarter of the dQ
+//              tile added to an fp32 accumulator with vector reductions.  At
+//              the end, dK and dV rows (TMEM lane = key) go out as bf16.
 // TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
 //               dK [384,448) dV [448,512).
 #include "table_eval.cuh"
@@ -37,8 +37,11 @@ namespace bam {
 namespace {
 
 constexpr int kBStages = 2;
-constexpr int kBThreads = 320;   // 8 element-wise warps, producer, MMA issuer
-constexpr int kBCompute = 8;
+constexpr int kBCompute = 16;   // element-wise warps: four per TMEM lane quarter
+constexpr int kBThreads = 32 * (kBCompute + 2);  // + producer + MMA issuer
+constexpr int kBProducerWarp = kBCompute;
+constexpr int kBMmaWarp = kBCompute + 1;
+constexpr int kBKeysPerWarp = 128 / (kBCompute / 4);  // 32 keys of the tile per thread
 constexpr int kTile = 128 * 64 * 2;  // 16 KB bf16 tile
 constexpr int kBWin = 256;
 
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     mbar_init(&sm.mma_final, 1);
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kBMmaWarp) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   const uint32_t tm = sm.tmem_base;
   const size_t plane = static_cast<size_t>(a.H) * a.tab_len;
 
-  if (warp == 8) {
+  if (warp == kBProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = (*ab == 0);
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       for (int t = max(0, issued - kBStages); t < issued; ++t)
         mbar_drain(&sm.qd_full[t % kBStages], (t / kBStages) & 1);
     }
-  } else if (warp == 9) {
+  } else if (warp == kBMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = (*ab == 0);
@@ -207,6 +210,17 @@ __global__ void __launch_bounds__(kBThreads, 1)
         ok = mbar_wait(&sm.ds_ready, t & 1, a.status, ab, kSiteBMmaDS);
         if (!ok) break;
         tc_fence_after();
+        // S and dP of the next tile first: their TMEM was read by the
+        // element-wise warps before ds_ready, and issuing them ahead of this
+        // tile's three gradient products lets the next tile's element-wise
+        // work overlap those products.
+        if (t + 1 < nq) {
+          ok = mbar_wait(&sm.qd_full[(t + 1) % kBStages], ((t + 1) / kBStages) & 1, a.status, ab,
+                         kSiteBMmaQD);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s_dp((t + 1) % kBStages);
+        }
         const uint32_t qa = smem_u32(sm.q[s]), da = smem_u32(sm.dO[s]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
@@ -222,13 +236,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
                   idQ, kk > 0 ? 1u : 0u);
         umma_commit(&sm.mma_done);
         umma_commit(&sm.qd_empty[s]);
-        if (t + 1 < nq) {
-          ok = mbar_wait(&sm.qd_full[(t + 1) % kBStages], ((t + 1) / kBStages) & 1, a.status, ab,
-                         kSiteBMmaQD);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s_dp((t + 1) % kBStages);
-        }
       }
       umma_commit(&sm.mma_final);
       mbar_drain(&sm.mma_final, 0);
@@ -236,7 +243,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   } else {
     // ------------------------------------------------------------ element-wise
     const int r = 32 * (warp & 3) + lane;  // query row within the tile = TMEM lane
-    const int hc = warp >> 2;              // which 64 keys of the tile
+    const int hc = warp >> 2;              // which 32 keys of the tile
     const uint32_t lb = tmem_lane_base(warp);
     const float s_h = a.ssmax ? __ldg(a.s + h) : 1.0f;
     // Scalar-gradient sums as f32x2 pairs (even / odd key columns):
@@ -247,31 +254,45 @@ __global__ void __launch_bounds__(kBThreads, 1)
     bool ok = (*ab == 0);
     auto dq_epilogue = [&](int t) {
       const int i = (q_first + t) * 128 + r;
-      uint32_t dv[32];
-      tmem_ld_32x32b_x32(tm + lb + kColDQ + 32 * hc, dv);
+      uint32_t dv[16];
+      tmem_ld_32x32b_x16(tm + lb + kColDQ + 16 * hc, dv);
       tmem_ld_wait();
-      reg_fence32(dv);
+      reg_fence16(dv);
       if (i < a.T) {
-        float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.T + i) * kHeadDim + 32 * hc;
+        float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.T + i) * kHeadDim + 16 * hc;
 #pragma unroll
-        for (int x = 0; x < 8; ++x)
+        for (int x = 0; x < 4; ++x)
           red_add_v4(dst + 4 * x, __uint_as_float(dv[4 * x]), __uint_as_float(dv[4 * x + 1]),
                      __uint_as_float(dv[4 * x + 2]), __uint_as_float(dv[4 * x + 3]));
       }
     };
+    // LSE and Delta of this thread's row, one query tile ahead.
+    float lse_nx = 0.f, del_nx = 0.f;
+    {
+      const int i = q_first * 128 + r;
+      if (nq > 0 && i < a.T) {
+        lse_nx = __ldg(a.lse + static_cast<size_t>(bh) * a.T + i);
+        del_nx = __ldg(a.delta + static_cast<size_t>(bh) * a.T + i);
+      }
+    }
     for (int t = 0; ok && t < nq; ++t) {
       const int s = t % kBStages;
       const int i0 = (q_first + t) * 128;
       const int i = i0 + r;
       const bool row_ok = i < a.T;
+      const float lse_row = lse_nx, del_row = del_nx;
+      if (t + 1 < nq && i + 128 < a.T) {
+        lse_nx = __ldg(a.lse + static_cast<size_t>(bh) * a.T + i + 128);
+        del_nx = __ldg(a.delta + static_cast<size_t>(bh) * a.T + i + 128);
+      }
       // Per-row constants.
       const float n = a.causal ? static_cast<float>(i + 1) : static_cast<float>(a.T);
       const float w_ln = logf(n) * 0.125f;             // ln(n_i)/sqrt(D)
       const float cn = a.ssmax ? s_h * w_ln : 0.125f;   // c_i
       const float cr = cn * 1.44269504088896341f;      // c_i log2(e)
       const size_t ridx = static_cast<size_t>(bh) * a.T + i;
-      const float lse2 = row_ok ? __ldg(a.lse + ridx) * 1.44269504088896341f : INFINITY;
-      const float delta = row_ok ? __ldg(a.delta + ridx) : 0.0f;
+      const float lse2 = row_ok ? lse_row * 1.44269504088896341f : INFINITY;
+      const float delta = row_ok ? del_row : 0.0f;
       int lim = a.T - 1 - j0;              // last visible key column
       if (a.causal) lim = min(lim, i - j0);
       const bool need_mask = lim < 127;
@@ -282,32 +303,25 @@ __global__ void __launch_bounds__(kBThreads, 1)
       if (!ok) break;
       ok = warp_wait(&sm.qd_full[s], (t / kBStages) & 1, a.status, ab, kSiteBWgQD);
       if (!ok) break;
-      if (t > 0) {
-        // Previous tile's MMAs are done: P^T / dS^T buffers and dS TMEM are
-        // free, and its dQ tile is ready.
-        ok = warp_wait(&sm.mma_done, (t - 1) & 1, a.status, ab, kSiteBWgDone);
-        if (!ok) break;
-        tc_fence_after();
-        dq_epilogue(t - 1);
-      }
       tc_fence_after();
       const float* wb = sm.win[s][0] + 128 + r;
       const float* wbeta = sm.win[s][1] + 128 + r;
       const float* wmu = sm.win[s][2] + 128 + r;
       // Row partial sums for the Delta correction and the SSMax sum.
       uint64_t pB2 = 0ull, pBeta2 = 0ull, pMu2 = 0ull, pS2 = 0ull, pDP2 = 0ull, rowSS2 = 0ull;
-      uint32_t pp[16], dd[16];
+      // Four 8-key chunks of S and dP per thread.
 #pragma unroll 1
-      for (int ch = 0; ch < 2; ++ch) {
-        const int c0 = 64 * hc + 32 * ch;
-        uint32_t sv[32], dpv[32];
-        tmem_ld_32x32b_x32(tm + lb + kColS + c0, sv);
-        tmem_ld_32x32b_x32(tm + lb + kColDP + c0, dpv);
+      for (int ch = 0; ch < 4; ++ch) {
+        const int c0 = kBKeysPerWarp * hc + 8 * ch;
+        uint32_t sv[8], dpv[8];
+        tmem_ld_32x32b_x8(tm + lb + kColS + c0, sv);
+        tmem_ld_32x32b_x8(tm + lb + kColDP + c0, dpv);
         tmem_ld_wait();
-        reg_fence32(sv);
-        reg_fence32(dpv);
+        reg_fence8(sv);
+        reg_fence8(dpv);
+        uint32_t pp[4], dd[4];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
+        for (int x = 0; x < 4; ++x) {
           const int c = c0 + 2 * x;
           const uint64_t s2 = f2_pack(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
           const uint64_t dp2 =
@@ -338,18 +352,25 @@ __global__ void __launch_bounds__(kBThreads, 1)
           f2_unpack(fmul2(dS2, cn2), q0, q1);
           dd[x] = pack_bf16x2(q0, q1);
         }
-        // P and c*dS, keys [c0, c0+32) of query row r, into the MN-major
-        // operands (four 16-byte chunks each) and c*dS into TMEM.
-#pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          const uint32_t off = mn_chunk_offset(c0 / 8 + q8, r);
-          *reinterpret_cast<uint4*>(sm.pt + off) =
-              make_uint4(pp[4 * q8], pp[4 * q8 + 1], pp[4 * q8 + 2], pp[4 * q8 + 3]);
-          *reinterpret_cast<uint4*>(sm.dst + off) =
-              make_uint4(dd[4 * q8], dd[4 * q8 + 1], dd[4 * q8 + 2], dd[4 * q8 + 3]);
+        if (ch == 0 && t > 0) {
+          // The previous tile's gradient products must be done before its
+          // P^T / dS^T buffers and dS TMEM are overwritten; its dQ tile is
+          // drained here, before this tile's dQ product is issued.
+          ok = warp_wait(&sm.mma_done, (t - 1) & 1, a.status, ab, kSiteBWgDone);
+          if (!ok) break;
+          tc_fence_after();
+          dq_epilogue(t - 1);
         }
-        tmem_st_32x32b_x16(tm + lb + kColDS + c0 / 2, dd);
+        // P and c*dS, keys [c0, c0+8) of query row r, into the MN-major
+        // operands (one 16-byte chunk each) and c*dS into TMEM.
+        {
+          const uint32_t off = mn_chunk_offset(c0 / 8, r);
+          *reinterpret_cast<uint4*>(sm.pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+          *reinterpret_cast<uint4*>(sm.dst + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+        }
+        tmem_st_32x32b_x4(tm + lb + kColDS + c0 / 2, dd);
       }
+      if (!ok) break;
       {
         float a0, a1;
         f2_unpack(rowSS2, a0, a1);
@@ -377,21 +398,21 @@ __global__ void __launch_bounds__(kBThreads, 1)
       if (ok) {
         tc_fence_after();
         dq_epilogue(nq - 1);
-        // dK and dV rows: TMEM lane = key j0 + r; this warp writes 32 of the
+        // dK and dV rows: TMEM lane = key j0 + r; this warp writes 16 of the
         // 64 dimensions.
         const int j = j0 + r;
         for (int which = 0; which < 2; ++which) {
-          const uint32_t col = (which ? kColDV : kColDK) + 32 * hc;
-          uint32_t kvv[32];
-          tmem_ld_32x32b_x32(tm + lb + col, kvv);
+          const uint32_t col = (which ? kColDV : kColDK) + 16 * hc;
+          uint32_t kvv[16];
+          tmem_ld_32x32b_x16(tm + lb + col, kvv);
           tmem_ld_wait();
-          reg_fence32(kvv);
+          reg_fence16(kvv);
           if (j < a.T) {
             uint16_t* out =
-                (which ? a.dv : a.dk) + (static_cast<size_t>(bh) * a.T + j) * kHeadDim + 32 * hc;
+                (which ? a.dv : a.dk) + (static_cast<size_t>(bh) * a.T + j) * kHeadDim + 16 * hc;
             uint4* o4 = reinterpret_cast<uint4*>(out);
 #pragma unroll
-            for (int x = 0; x < 4; ++x)
+            for (int x = 0; x < 2; ++x)
               o4[x] = make_uint4(
                   pack_bf16x2(__uint_as_float(kvv[8 * x]), __uint_as_float(kvv[8 * x + 1])),
                   pack_bf16x2(__uint_as_float(kvv[8 * x + 2]), __uint_as_float(kvv[8 * x + 3])),
@@ -430,7 +451,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   tc_fence_before();
   __syncthreads();
   grid_dep_trigger();
-  if (warp == 9) {
+  if (warp == kBMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tm, 512);
   }
