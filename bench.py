@@ -182,13 +182,12 @@ def run_ours(args, rank, world, dev, torch, dist):
     g = [torch.empty(H, dtype=torch.float32, device=dev) for _ in range(4)]
     ws_f = ba.workspace(ba.BAM_OP_FWD, B, H, T, dev)
     ws_b = ba.workspace(ba.BAM_OP_BWD, B, H, T, dev)
-    stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
 
     def step(q, k, v, do):
-        ba.bam_attn_fwd(q, k, v, o, lse, prm, ws_f, stream)
-        ba.bam_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, g[0], g[1], g[2], g[3], prm, ws_b,
-                        stream)
+        # current stream at call time (the capture stream while capturing)
+        ba.bam_attn_fwd(q, k, v, o, lse, prm, ws_f)
+        ba.bam_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, g[0], g[1], g[2], g[3], prm, ws_b)
 
     for _ in range(args.warmup):
         step(t["q"], t["k"], t["v"], t["do"])
@@ -196,31 +195,47 @@ def run_ours(args, rank, world, dev, torch, dist):
     if ba.bam_attn_check_status(ws_b) != ba.BAM_OK or ba.bam_attn_check_status(ws_f) != ba.BAM_OK:
         raise RuntimeError("device status not clean after warm-up")
 
+    # The step's launches (two C-ABI calls, five kernels) are captured once
+    # into a CUDA graph and replayed, so that host launch latency does not
+    # leave the GPU idle between kernels.
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+
+    def capture(fn):
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            fn()  # one eager call on the capture stream first
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g_, stream=side):
+            fn()
+        torch.cuda.synchronize()
+        return g_
+
+    launches0 = ba.bam_attn_launch_count()
+    graph = capture(lambda: step(t["q"], t["k"], t["v"], t["do"]))
+    launches_per_step = (ba.bam_attn_launch_count() - launches0) // 2
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
     # Device-timed steps; L2 flushed between steps (outside the events).
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    kev = {k: hook_events(torch, args.steps) for k in (ba.BAM_KERNEL_FWD, ba.BAM_KERNEL_BWD)}
-    launches0 = ba.bam_attn_launch_count()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         for i in range(args.steps):
             flush.zero_()
-            for k, lst in kev.items():
-                ba.bam_attn_profile_events(k, lst[i][0], lst[i][1])
-            ev[i][0].record(stream)
-            step(t["q"], t["k"], t["v"], t["do"])
-            ev[i][1].record(stream)
+            ev[i][0].record()
+            graph.replay()
+            ev[i][1].record()
         torch.cuda.synchronize()
-    for k in kev:
-        ba.bam_attn_profile_events(k, None, None)
-    launches = ba.bam_attn_launch_count() - launches0
     if world > 1:
         dist.barrier()
+    launches = launches_per_step * args.steps
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
-    kern_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in lst) for k, lst in kev.items()}
     if world > 1:
         tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -228,8 +243,28 @@ def run_ours(args, rank, world, dev, torch, dist):
     flops_step = train_flops(B, H, T)
     value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
 
+    # Per-kernel durations: a second graph of the same step whose kernels are
+    # bracketed by the library's event hook (event-record nodes in the graph).
+    kinds = (ba.BAM_KERNEL_TABLE, ba.BAM_KERNEL_FWD, ba.BAM_KERNEL_BWD_PREP, ba.BAM_KERNEL_BWD,
+             ba.BAM_KERNEL_BWD_FINAL)
+    kev = {k: hook_events(torch, 1)[0] for k in kinds}
+    for k, (b0, b1) in kev.items():
+        ba.bam_attn_profile_events(k, b0, b1)
+    kgraph = capture(lambda: step(t["q"], t["k"], t["v"], t["do"]))
+    for k in kinds:
+        ba.bam_attn_profile_events(k, None, None)
+    kms = {k: [] for k in kinds}
+    for i in range(args.steps):
+        flush.zero_()
+        kgraph.replay()
+        torch.cuda.synchronize()
+        for k, (b0, b1) in kev.items():
+            kms[k].append(b0.elapsed_time(b1))
+    kern_ms = {k: statistics.mean(v) for k, v in kms.items()}
+
     # End to end through the C ABI with host buffers: H2D of the step's
-    # inputs from pinned memory, fwd+bwd, D2H of the gradients, every step.
+    # inputs from pinned memory, fwd+bwd, D2H of the gradients, every step
+    # (captured into a graph the same way).
     host_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
     dev_in = {n: torch.empty_like(t[n]) for n in host_in}
     host_out = [torch.empty_like(x, device="cpu").pin_memory() for x in (dq, dk, dv)]
@@ -244,16 +279,17 @@ def run_ours(args, rank, world, dev, torch, dist):
         for hst, src in zip(host_out + host_g, [dq, dk, dv] + g):
             hst.copy_(src, non_blocking=True)
 
+    egraph = capture(e2e_step)
     for _ in range(max(2, args.warmup)):
-        e2e_step()
+        egraph.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_ms = 0.0
     for _ in range(args.steps):
         flush.zero_()
-        e0.record(stream)
-        e2e_step()
-        e1.record(stream)
+        e0.record()
+        egraph.replay()
+        e1.record()
         e1.synchronize()
         e_ms += e0.elapsed_time(e1)
     if world > 1:
@@ -277,8 +313,11 @@ def run_ours(args, rank, world, dev, torch, dist):
             "traffic": profiled_traffic("bam_bwd_kernel" if dom == ba.BAM_KERNEL_BWD
                                         else "bam_fwd_kernel"),
             "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
-            "kernel_ms": {"fwd": round(kern_ms[ba.BAM_KERNEL_FWD], 4),
-                          "bwd": round(kern_ms[ba.BAM_KERNEL_BWD], 4)},
+            "kernel_ms": {"table": round(kern_ms[ba.BAM_KERNEL_TABLE], 4),
+                          "fwd": round(kern_ms[ba.BAM_KERNEL_FWD], 4),
+                          "bwd_prep": round(kern_ms[ba.BAM_KERNEL_BWD_PREP], 4),
+                          "bwd": round(kern_ms[ba.BAM_KERNEL_BWD], 4),
+                          "bwd_final": round(kern_ms[ba.BAM_KERNEL_BWD_FINAL], 4)},
             "fwd_frac": round(fwd_flops / (kern_ms[ba.BAM_KERNEL_FWD] * 1e-3) / 1e12 / peak, 4)}
 
     line = {
@@ -290,6 +329,7 @@ def run_ours(args, rank, world, dev, torch, dist):
         "config": {"workload": "train_B8_H12_T512", "B": B, "H": H, "T": T, "D": D,
                    "causal": True, "ssmax": True, "step": "fwd+bwd",
                    "l2": "flushed (256 MB write) between timed steps",
+                   "launch": "CUDA graph of the two C-ABI calls, replayed per step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

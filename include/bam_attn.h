@@ -146,8 +146,9 @@ enum {
 };
 
 /* Instrumentation: while set, every launch of kernel `which` is bracketed
- * by cudaEventRecord(before) / cudaEventRecord(after) on the launch stream.
- * Pass NULL events to clear.  Not thread-safe with concurrent callers. */
+ * by records of `before` and `after` on the launch stream (external records,
+ * so that a captured CUDA graph keeps them as event-record nodes).  Pass
+ * NULL events to clear.  Not thread-safe with concurrent callers. */
 bam_status bam_attn_profile_events(int which, cudaEvent_t before, cudaEvent_t after);
 
 /* Number of kernel launches the library has issued since load (all kinds). */

@@ -29,14 +29,24 @@ cudaError_t launch_kernel(int which, cudaStream_t st, F launch) {
     before = g_prof_before[which];
     after = g_prof_after[which];
   }
+  // Under stream capture the records are external, so that they become
+  // event-record nodes of the graph (timestamps on every replay) rather than
+  // internal dependencies.
+  unsigned flags = cudaEventRecordDefault;
+  if (before || after) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs == cudaStreamCaptureStatusActive) flags = cudaEventRecordExternal;
+  }
   if (before) {
-    cudaError_t e = cudaEventRecord(before, st);
+    cudaError_t e = cudaEventRecordWithFlags(before, st, flags);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = launch();
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e != cudaSuccess) return e;
-  if (after) e = cudaEventRecord(after, st);
+  if (after) e = cudaEventRecordWithFlags(after, st, flags);
   return e;
 }
 
@@ -68,6 +78,23 @@ bool encode_rows(CUtensorMap* m, const void* base, int BH, int T) {
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// fp32 [BH, T, 64] accumulator as a 3-D tensor (64, T, BH) in 32 x 128
+// boxes (128-byte rows, 128-byte swizzle) for TMA reductions.
+bool encode_acc_rows(CUtensorMap* m, void* base, int BH, int T) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 4,
+                           static_cast<cuuint64_t>(T) * kHeadDim * 4};
+  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -324,8 +351,10 @@ bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void*
   cudaError_t e =
       launch_kernel(BAM_KERNEL_BWD_PREP, stream, [&] { return launch_bwd_prep(ba, stream); });
   if (e != cudaSuccess) return BAM_ERR_CUDA;
+  CUtensorMap tdq;
+  if (!encode_acc_rows(&tdq, ba.dq_acc, BH, T)) return BAM_ERR_CUDA;
   e = launch_kernel(BAM_KERNEL_BWD, stream,
-                    [&] { return launch_bwd(tq, tk, tv, tdo, ba, stream); });
+                    [&] { return launch_bwd(tq, tk, tv, tdo, tdq, ba, stream); });
   if (e != cudaSuccess) return BAM_ERR_CUDA;
   e = launch_kernel(BAM_KERNEL_BWD_FINAL, stream, [&] { return launch_bwd_final(ba, stream); });
   return cuda_status(e);

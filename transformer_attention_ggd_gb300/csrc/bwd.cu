@@ -26,9 +26,10 @@
 //   warps 0-15 four warps per TMEM lane quarter; each thread owns one query
 //              row and one quarter (32 keys) of the tile: P, dS, the scalar-
 //              gradient sums (as f32x2 pairs of partial sums), P and c*dS to
-//              shared memory and c*dS to TMEM, then its quarter of the dQ
-//              tile added to an fp32 accumulator with vector reductions.  At
-//              the end, dK and dV rows (TMEM lane = key) go out as bf16.
+//              shared memory and c*dS to TMEM; the finished dQ tile goes
+//              through a shared staging tile into the fp32 accumulator with
+//              TMA reductions.  At the end, dK and dV rows (TMEM lane = key)
+//              go out as bf16.
 // TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
 //               dK [384,448) dV [448,512).
 #include "table_eval.cuh"
@@ -52,6 +53,7 @@ struct __align__(1024) BwdSmem {
   uint8_t dO[kBStages][kTile];
   uint8_t pt[2 * kTile];   // P^T as an MN-major A operand: 2 atoms of 64 keys x 128 queries
   uint8_t dst[2 * kTile];  // (c dS)^T, same layout
+  float dqs[2][128][32];   // dQ tile staged for the TMA reduction: two 128-B-swizzled boxes
   float win[kBStages][3][kBWin];
   float red[kBCompute][4];
   uint64_t kv_full;
@@ -102,7 +104,7 @@ __device__ __forceinline__ uint32_t mn_chunk_offset(int m8, int k) {
 __global__ void __launch_bounds__(kBThreads, 1)
     bam_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                   const BwdArgs a) {
+                   const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
@@ -252,18 +254,30 @@ __global__ void __launch_bounds__(kBThreads, 1)
     uint64_t accB2 = 0ull, accBeta2 = 0ull, accMu2 = 0ull;
     float acc_s = 0.f;
     bool ok = (*ab == 0);
+    // dQ of a finished query tile: TMEM -> shared staging tile -> one TMA
+    // reduction (add) per 32-column box into the fp32 accumulator.  Rows past
+    // T are clipped by the tensor map.
     auto dq_epilogue = [&](int t) {
-      const int i = (q_first + t) * 128 + r;
       uint32_t dv[16];
       tmem_ld_32x32b_x16(tm + lb + kColDQ + 16 * hc, dv);
       tmem_ld_wait();
       reg_fence16(dv);
-      if (i < a.T) {
-        float* dst = a.dq_acc + (static_cast<size_t>(bh) * a.T + i) * kHeadDim + 16 * hc;
+      if (threadIdx.x == 0) bulk_wait_read_all();  // previous reduction has read the tile
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * kBCompute) : "memory");
+      uint8_t* box = reinterpret_cast<uint8_t*>(sm.dqs[hc >> 1]);
 #pragma unroll
-        for (int x = 0; x < 4; ++x)
-          red_add_v4(dst + 4 * x, __uint_as_float(dv[4 * x]), __uint_as_float(dv[4 * x + 1]),
-                     __uint_as_float(dv[4 * x + 2]), __uint_as_float(dv[4 * x + 3]));
+      for (int x = 0; x < 4; ++x) {
+        const int c = 4 * (hc & 1) + x;  // 16-byte chunk of the 128-byte row
+        *reinterpret_cast<uint4*>(box + r * 128 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(dv[4 * x], dv[4 * x + 1], dv[4 * x + 2], dv[4 * x + 3]);
+      }
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * kBCompute) : "memory");
+      if (threadIdx.x == 0) {
+        const int i0 = (q_first + t) * 128;
+        tma_reduce_add_3d(&tdq, sm.dqs[0], 0, i0, bh);
+        tma_reduce_add_3d(&tdq, sm.dqs[1], 32, i0, bh);
+        bulk_commit();
       }
     };
     // LSE and Delta of this thread's row, one query tile ahead.
@@ -422,6 +436,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         }
       }
     }
+    if (threadIdx.x == 0) bulk_wait_all();  // dQ reductions complete before exit
     // Block reduction of the scalar-gradient sums, one atomic per head and sum.
     float v4[4];
     {
@@ -596,7 +611,8 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
+                       cudaStream_t st) {
   const size_t smem = sizeof(BwdSmem) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -608,7 +624,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   }
   const unsigned grid = static_cast<unsigned>(a.nkb) * static_cast<unsigned>(a.B * a.H);
   return launch_k(bam_bwd_kernel, dim3(grid), dim3(kBThreads), smem, st, true, tq, tk, tv, tdo,
-                  a);
+                  tdq, a);
 }
 
 cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
