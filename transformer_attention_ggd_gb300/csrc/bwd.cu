@@ -487,36 +487,39 @@ __global__ void __launch_bounds__(256) bam_bwd_prep_kernel(const BwdArgs a, int 
   const size_t rows = static_cast<size_t>(a.B) * a.H * a.T;
   const size_t tid = static_cast<size_t>(blockIdx.x - table_blocks) * blockDim.x + threadIdx.x;
   const size_t nthreads = static_cast<size_t>(gridDim.x - table_blocks) * blockDim.x;
-  for (size_t row = tid; row < rows; row += nthreads) {
-    const uint4* g = reinterpret_cast<const uint4*>(a.dO + row * kHeadDim);
+  grid_dep_wait();  // O comes from the forward
+  // Delta: eight threads per row, eight elements each, shuffle reduction.
+  // The loop bound is warp-uniform so that every lane reaches the shuffles.
+  const int sub = threadIdx.x & 7;
+  for (size_t wb = tid & ~static_cast<size_t>(31); wb < rows * 8; wb += nthreads) {
+    const size_t row = (wb + (threadIdx.x & 31)) / 8;
     float acc = 0.f;
-    if (a.o_fp32) {
-      const float4* o = reinterpret_cast<const float4*>(static_cast<const float*>(a.o) + row * kHeadDim);
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const uint4 w = g[x];
-        const float4 o0 = o[2 * x], o1 = o[2 * x + 1];
-        acc += __uint_as_float(w.x << 16) * o0.x + __uint_as_float(w.x & 0xFFFF0000u) * o0.y +
-               __uint_as_float(w.y << 16) * o0.z + __uint_as_float(w.y & 0xFFFF0000u) * o0.w +
-               __uint_as_float(w.z << 16) * o1.x + __uint_as_float(w.z & 0xFFFF0000u) * o1.y +
-               __uint_as_float(w.w << 16) * o1.z + __uint_as_float(w.w & 0xFFFF0000u) * o1.w;
+    if (row < rows) {
+      const uint4 w = reinterpret_cast<const uint4*>(a.dO + row * kHeadDim)[sub];
+      float o[8];
+      if (a.o_fp32) {
+        const float4* op = reinterpret_cast<const float4*>(static_cast<const float*>(a.o) +
+                                                           row * kHeadDim) + 2 * sub;
+        const float4 o0 = op[0], o1 = op[1];
+        o[0] = o0.x; o[1] = o0.y; o[2] = o0.z; o[3] = o0.w;
+        o[4] = o1.x; o[5] = o1.y; o[6] = o1.z; o[7] = o1.w;
+      } else {
+        const uint4 u = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) +
+                                                       row * kHeadDim)[sub];
+        o[0] = __uint_as_float(u.x << 16); o[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        o[4] = __uint_as_float(u.z << 16); o[5] = __uint_as_float(u.z & 0xFFFF0000u);
+        o[6] = __uint_as_float(u.w << 16); o[7] = __uint_as_float(u.w & 0xFFFF0000u);
       }
-    } else {
-      const uint4* o = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.o) + row * kHeadDim);
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const uint4 w = g[x], u = o[x];
-        acc += __uint_as_float(w.x << 16) * __uint_as_float(u.x << 16) +
-               __uint_as_float(w.x & 0xFFFF0000u) * __uint_as_float(u.x & 0xFFFF0000u) +
-               __uint_as_float(w.y << 16) * __uint_as_float(u.y << 16) +
-               __uint_as_float(w.y & 0xFFFF0000u) * __uint_as_float(u.y & 0xFFFF0000u) +
-               __uint_as_float(w.z << 16) * __uint_as_float(u.z << 16) +
-               __uint_as_float(w.z & 0xFFFF0000u) * __uint_as_float(u.z & 0xFFFF0000u) +
-               __uint_as_float(w.w << 16) * __uint_as_float(u.w << 16) +
-               __uint_as_float(w.w & 0xFFFF0000u) * __uint_as_float(u.w & 0xFFFF0000u);
-      }
+      acc = __uint_as_float(w.x << 16) * o[0] + __uint_as_float(w.x & 0xFFFF0000u) * o[1] +
+            __uint_as_float(w.y << 16) * o[2] + __uint_as_float(w.y & 0xFFFF0000u) * o[3] +
+            __uint_as_float(w.z << 16) * o[4] + __uint_as_float(w.z & 0xFFFF0000u) * o[5] +
+            __uint_as_float(w.w << 16) * o[6] + __uint_as_float(w.w & 0xFFFF0000u) * o[7];
     }
-    a.delta[row] = acc;
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (sub == 0 && row < rows) a.delta[row] = acc;
   }
   float4* dq4 = reinterpret_cast<float4*>(a.dq_acc);
   const size_t n4 = rows * (kHeadDim / 4);
@@ -599,9 +602,9 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
 
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st) {
   const size_t rows = static_cast<size_t>(a.B) * a.H * a.T;
-  size_t want = (rows * 16 + 255) / 256;
+  size_t want = (rows * 8 + 255) / 256;
   if (want < 1) want = 1;
-  if (want > 152 * 8) want = 152 * 8;
+  if (want > 152 * 4) want = 152 * 4;
   const size_t tab_entries = static_cast<size_t>(a.tab.H) * a.tab.len;
   size_t tb = (tab_entries + 255) / 256;
   if (tb > 152 * 2) tb = 152 * 2;
@@ -632,7 +635,7 @@ cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
   const size_t items = static_cast<size_t>(a.B) * a.H * ((a.T + kFinalRows - 1) / kFinalRows);
   size_t want = (n8 + 255) / 256;
   if (want < items) want = items;
-  if (want > 152 * 8) want = 152 * 8;
+  if (want > 152 * 2) want = 152 * 2;
   const unsigned grid = static_cast<unsigned>(want);
   return launch_k(bam_bwd_final_kernel, dim3(grid), dim3(256), 0, st, true, a);
 }

@@ -9,8 +9,9 @@
 // relative distance follows the Sandwich entry of the attention-gym
 // "Score Mods" page.
 //
-// Values are computed in fp64 and stored in fp32, pre-multiplied by log2(e)
-// so that the softmax can run on exp2.  The backward mode also writes
+// Values are computed in fp32 with an error-compensated exponent (see
+// table_eval.cuh) and stored pre-multiplied by log2(e) so that the softmax
+// can run on exp2.  The backward mode also writes
 // db/dbeta and db/dmu (natural units):
 //   db/dbeta = b * ln(u / alpha)
 //   db/dmu   = -beta * b * sgn(d - mu) / u      (0 inside the eps clamp)

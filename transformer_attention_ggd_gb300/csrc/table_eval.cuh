@@ -6,14 +6,14 @@
 
 namespace bam {
 
-// b, db/dbeta and db/dmu at distance d.  fp32 arithmetic except for the
-// exponent y = beta * log2(u / alpha), which is assembled in double from the
-// exact binary exponent of u/alpha and an fp32 log2 of its mantissa (absolute
-// error ~1e-7); 2^y is then an exact power of two times exp2f of the
-// fractional part.  The relative error of b is a few 1e-7 whatever its
+// b, db/dbeta and db/dmu at distance d, in fp32 arithmetic only (fp64 is slow
+// on this GPU).  The exponent y = beta * log2(u / alpha) is carried as an
+// unevaluated sum of two floats: log2(u/alpha) = e + log2(m) with the exact
+// binary exponent e and the mantissa m in [0.5, 1) (log2f(m) has an absolute
+// error ~6e-8), the products beta*e and beta*log2(m) are split exactly with
+// fma, and the sum with TwoSum.  2^y is then 2^n (exact) times exp2f of the
+// small remainder, so the relative error of b stays a few 1e-7 at any
 // magnitude, where a plain fp32 pow loses ~1e-7 * |y| (1e-6 at |b| ~ 1e4).
-// The few double operations per entry keep the table cheap on a GPU whose
-// fp64 rate is low.
 __device__ __forceinline__ void bias_terms(int dint, float alpha, float beta, float mu, float eps,
                                            float* b, float* dbeta, float* dmu) {
   float u = fabsf(static_cast<float>(dint) - mu);
@@ -30,15 +30,24 @@ __device__ __forceinline__ void bias_terms(int dint, float alpha, float beta, fl
   }
   const float r = __fdiv_rn(u, alpha);
   int e2 = 0;
-  const float mant = frexpf(r, &e2);                               // r = mant * 2^e2
-  const double L = static_cast<double>(e2) + static_cast<double>(log2f(mant));  // log2(r)
-  double y = static_cast<double>(beta) * L;
-  y = fmin(fmax(y, -400.0), 400.0);
-  const double n = floor(y);
-  const float pw = ldexpf(exp2f(static_cast<float>(y - n)), static_cast<int>(n));  // 2^y
+  const float mant = frexpf(r, &e2);  // r = mant * 2^e2
+  const float lm = log2f(mant);
+  const float fe = static_cast<float>(e2);
+  // beta * fe and beta * lm with their rounding errors
+  const float p1 = beta * fe, q1 = fmaf(beta, fe, -p1);
+  const float p2 = beta * lm, q2 = fmaf(beta, lm, -p2);
+  // TwoSum of p1 + p2
+  const float sh = p1 + p2;
+  const float bv = sh - p1;
+  const float sl = (p1 - (sh - bv)) + (p2 - bv);
+  float yh = sh, yl = sl + q1 + q2;  // y = yh + yl
+  yh = fminf(fmaxf(yh, -400.0f), 400.0f);
+  const float n = floorf(yh);
+  const float f = (yh - n) + yl;  // yh - n is exact
+  const float pw = ldexpf(exp2f(f), static_cast<int>(n));  // 2^y
   const float bb = -pw;
   *b = bb;
-  *dbeta = static_cast<float>(static_cast<double>(bb) * L * 0.69314718055994530942);  // b ln r
+  *dbeta = bb * ((fe + lm) * 0.69314718055994530942f);  // b ln r
   const float sgn = (static_cast<float>(dint) - mu > 0.0f) ? 1.0f : -1.0f;
   *dmu = clamped ? 0.0f : -beta * bb * sgn / u;
 }
