@@ -170,6 +170,7 @@ def make_train_inputs(torch, dev, seed=None):
 
 def run_ours(args, rank, world, dev, torch, dist):
     from transformer_attention_ggd_gb300 import bam_attn as ba
+    from transformer_attention_ggd_gb300.dist_utils import max_over_ranks
 
     ba.load_library()
     peaks = load_peaks()
@@ -237,9 +238,7 @@ def run_ours(args, rank, world, dev, torch, dist):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
     if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, dist, dev)
     flops_step = train_flops(B, H, T)
     value = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
 
@@ -293,9 +292,7 @@ def run_ours(args, rank, world, dev, torch, dist):
         e1.synchronize()
         e_ms += e0.elapsed_time(e1)
     if world > 1:
-        tt = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e_ms = float(tt.item())
+        e_ms = max_over_ranks(e_ms, dist, dev)
     e2e_value = flops_step * args.steps * world / (e_ms * 1e-3) / 1e12
 
     # Roofline of the dominant kernel (the fused backward): algorithmic
