@@ -57,6 +57,8 @@ struct __align__(1024) BwdSmem {
   float win[kBStages][3][kBWin];
   float red[kBCompute][4];
   uint64_t kv_full;
+  uint64_t dqs_full;
+  uint64_t dqs_free;
   uint64_t qd_full[kBStages];
   uint64_t qd_empty[kBStages];
   uint64_t s_full;
@@ -74,7 +76,8 @@ enum : int {
   kSiteBMmaDS = 62,
   kSiteBWgS = 70,
   kSiteBWgQD = 71,
-  kSiteBWgDone = 72
+  kSiteBWgDone = 72,
+  kSiteBWgDq = 73
 };
 
 constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 320, kColDK = 384,
@@ -131,6 +134,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.ds_ready, kBCompute);
+    mbar_init(&sm.dqs_full, kBCompute);
+    mbar_init(&sm.dqs_free, 1);
     mbar_init(&sm.mma_done, 1);
     mbar_init(&sm.mma_final, 1);
     fence_barrier_init();
@@ -256,29 +261,43 @@ __global__ void __launch_bounds__(kBThreads, 1)
     bool ok = (*ab == 0);
     // dQ of a finished query tile: TMEM -> shared staging tile -> one TMA
     // reduction (add) per 32-column box into the fp32 accumulator.  Rows past
-    // T are clipped by the tensor map.
-    auto dq_epilogue = [&](int t) {
+    // T are clipped by the tensor map.  Hand-offs use bounded mbarrier waits
+    // (never a hardware barrier), so that a warp that gives up cannot leave the
+    // others blocked: thread 0 releases the staging tile once the previous
+    // reduction has read it (dqs_free), every warp arrives once its part is
+    // written (dqs_full), and thread 0 then issues the reduction.
+    int n_dq = 0;  // dQ tiles staged so far
+    auto dq_epilogue = [&](int t) -> bool {
       uint32_t dv[16];
       tmem_ld_32x32b_x16(tm + lb + kColDQ + 16 * hc, dv);
       tmem_ld_wait();
       reg_fence16(dv);
-      if (threadIdx.x == 0) bulk_wait_read_all();  // previous reduction has read the tile
-      asm volatile("bar.sync 2, %0;" ::"n"(32 * kBCompute) : "memory");
+      if (n_dq > 0) {
+        if (threadIdx.x == 0) {
+          bulk_wait_read_all();
+          mbar_arrive(&sm.dqs_free);
+        }
+        if (!warp_wait(&sm.dqs_free, (n_dq - 1) & 1, a.status, ab, kSiteBWgDq)) return false;
+      }
       uint8_t* box = reinterpret_cast<uint8_t*>(sm.dqs[hc >> 1]);
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const int c = 4 * (hc & 1) + x;  // 16-byte chunk of the 128-byte row
-        *reinterpret_cast<uint4*>(box + r * 128 + ((c ^ (r & 7)) << 4)) =
+        const int cc = 4 * (hc & 1) + x;  // 16-byte chunk of the 128-byte row
+        *reinterpret_cast<uint4*>(box + r * 128 + ((cc ^ (r & 7)) << 4)) =
             make_uint4(dv[4 * x], dv[4 * x + 1], dv[4 * x + 2], dv[4 * x + 3]);
       }
       fence_proxy_async_smem();
-      asm volatile("bar.sync 2, %0;" ::"n"(32 * kBCompute) : "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.dqs_full);
       if (threadIdx.x == 0) {
+        if (!mbar_wait(&sm.dqs_full, n_dq & 1, a.status, ab, kSiteBWgDq)) return false;
         const int i0 = (q_first + t) * 128;
         tma_reduce_add_3d(&tdq, sm.dqs[0], 0, i0, bh);
         tma_reduce_add_3d(&tdq, sm.dqs[1], 32, i0, bh);
         bulk_commit();
       }
+      ++n_dq;
+      return true;
     };
     // LSE and Delta of this thread's row, one query tile ahead.
     float lse_nx = 0.f, del_nx = 0.f;
@@ -373,7 +392,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
           ok = warp_wait(&sm.mma_done, (t - 1) & 1, a.status, ab, kSiteBWgDone);
           if (!ok) break;
           tc_fence_after();
-          dq_epilogue(t - 1);
+          if (!dq_epilogue(t - 1)) {
+            ok = false;
+            break;
+          }
         }
         // P and c*dS, keys [c0, c0+8) of query row r, into the MN-major
         // operands (one 16-byte chunk each) and c*dS into TMEM.
@@ -411,7 +433,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
       ok = warp_wait(&sm.mma_done, (nq - 1) & 1, a.status, ab, kSiteBWgDone);
       if (ok) {
         tc_fence_after();
-        dq_epilogue(nq - 1);
+        ok = dq_epilogue(nq - 1);
+      }
+      if (ok) {
         // dK and dV rows: TMEM lane = key j0 + r; this warp writes 16 of the
         // 64 dimensions.
         const int j = j0 + r;
