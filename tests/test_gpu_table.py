@@ -1,11 +1,13 @@
 """The per-head distance table against the oracle's bias, entry by entry.
 
 The forward writes b_h(d) * log2(e) for every distance its tiles can touch
-into the workspace right after the 256 status bytes: H rows of `len`
-entries, entry x holding d = x - off (len, off as laid out by the library:
-off = 256 causal, round_up(T,256) + 256 otherwise; len = off +
-round_up(T,256) + 256).  fp32 storage of an fp32-evaluated value with a
-compensated exponent: relative error <= 1e-6 against the fp64 oracle.
+into the workspace right after the 256 status bytes.  Rows are stored
+reversed, in four copies each shifted by one more entry: copy k holds H rows
+of `len` entries, entry y of a row holding table index x = len - 1 - y + k,
+i.e. d = x - off (0 where x >= len), with off = 256 causal,
+round_up(T,256) + 256 otherwise and len = off + round_up(T,256) + 256.
+fp32 storage of an fp32-evaluated value with a compensated exponent:
+relative error <= 1e-6 against the fp64 oracle.
 """
 
 import math
@@ -47,13 +49,19 @@ def test_distance_table_matches_oracle_bias(causal):
     t256 = (T + 255) // 256 * 256
     off = 256 if causal else t256 + 256
     length = off + t256 + 256
-    tab = ws[256:256 + H * length * 4].cpu().numpy().view(np.float32).reshape(H, length)
+    copies = ws[256:256 + 4 * H * length * 4].cpu().numpy().view(np.float32)
+    copies = copies.reshape(4, H, length)
     log2e = 1.0 / math.log(2.0)
     worst = 0.0
     for h in range(H):
         ref = np.array([oracle.bias(x - off, prm["alpha"][h], prm["beta"][h], prm["mu"][h])
                         for x in range(length)]) * log2e
         ref = np.maximum(ref, -3.0e38)
-        err = np.abs(tab[h] - ref) / np.maximum(np.abs(ref), 1e-30)
+        tab = copies[0, h, ::-1]  # copy 0 reversed back: entry x
+        err = np.abs(tab - ref) / np.maximum(np.abs(ref), 1e-30)
         worst = max(worst, float(err.max()))
-        assert err.max() <= 1e-6, (h, int(err.argmax()), tab[h][err.argmax()], ref[err.argmax()])
+        assert err.max() <= 1e-6, (h, int(err.argmax()), tab[err.argmax()], ref[err.argmax()])
+        for k in range(1, 4):
+            # copy k is copy 0 shifted by k entries, zero-filled at the front
+            assert np.array_equal(copies[k, h, k:], copies[0, h, :length - k]), (h, k)
+            assert np.all(copies[k, h, :k] == 0.0), (h, k)

@@ -129,7 +129,7 @@ FwdWs fwd_ws(int H, int T, int causal) {
   const TableGeom g = table_geom(T, causal);
   FwdWs w;
   w.table = kStatusBytes;
-  w.total = w.table + align256(static_cast<size_t>(H) * g.len * 4);
+  w.total = w.table + align256((kTabCopies * static_cast<size_t>(H) * g.len + kTabPadFloats) * 4);
   return w;
 }
 
@@ -141,7 +141,8 @@ BwdWs bwd_ws(int B, int H, int T, int causal) {
   const size_t BH = static_cast<size_t>(B) * H;
   BwdWs w;
   w.table = kStatusBytes;
-  w.delta = w.table + align256(3 * static_cast<size_t>(H) * g.len * 4);
+  w.delta =
+      w.table + align256((3 * kTabCopies * static_cast<size_t>(H) * g.len + kTabPadFloats) * 4);
   w.dq_acc = w.delta + align256(BH * T * 4);
   w.rowacc = w.dq_acc + align256(BH * T * kHeadDim * 4);
   w.gacc = w.rowacc + align256(BH * T * 8 * 4);

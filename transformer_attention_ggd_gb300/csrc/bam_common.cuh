@@ -22,10 +22,27 @@ constexpr size_t kStatusBytes = 256;
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Per-head distance table (forward / backward): entry x of head h holds
-// b_h(d) * log2(e) for d = x - off.  Entries exist for every d that a
-// 128 x 256 tile window can touch; all windows start at a multiple of 128
-// entries, so their byte offsets are 512-byte aligned.
+// Per-head distance table (forward / backward): b_h(d) * log2(e) for every
+// d that a tile window can touch, d = x - off for a table index x in
+// [0, len).  In memory each row is stored reversed, in kTabCopies copies:
+// entry y of copy k of head h holds index x = len - 1 - y + k (0 where that
+// falls past the row).  A thread whose row meets key columns c, c+1, c+2,
+// c+3 needs d, d-1, d-2, d-3, i.e. four consecutive reversed entries; in the
+// copy k = (its row + 1) mod 4 they start on a 16-byte boundary, so one
+// vector load fetches them.  Windows start at multiples of 128 entries.
+constexpr int kTabCopies = 4;
+// Window copies may read up to three entries past the end of a row (never
+// used); the table region is padded so the last row stays inside it.
+constexpr int kTabPadFloats = 16;
+
+// Offset (floats) of window copy k in shared memory when copies are
+// `stride` floats apart (stride a multiple of 32): extra shifts of 0, 4, 12
+// and 20 floats spread the 16-byte loads of the eight lanes of each quarter
+// warp over all 32 banks.
+__host__ __device__ constexpr int win_copy_off(int k, int stride) {
+  return k * stride + (k ? 8 * k - 4 : 0);
+}
+
 struct TableGeom {
   int off;  // index of d = 0
   int len;  // entries per head, multiple of 256
@@ -48,7 +65,7 @@ enum TableMode : int {
 };
 
 struct TableArgs {
-  float* tab;  // [ntables][H][len]
+  float* tab;  // decode: [H][len]; by distance: [ntables][kTabCopies][H][len] reversed rows
   const float* alpha;
   const float* beta;
   const float* mu;

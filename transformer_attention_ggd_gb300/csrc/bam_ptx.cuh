@@ -347,6 +347,15 @@ __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
+
+// Four consecutive fp32 values from a 16-byte aligned address as two f32x2
+// pairs (values 0,1 and 2,3): one vector load.
+__device__ __forceinline__ void ld_f2x2(const float* p, uint64_t& a, uint64_t& b) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  a = f2_pack(v.x, v.y);
+  b = f2_pack(v.z, v.w);
+}
+
 __device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }

@@ -19,7 +19,8 @@
 // One CTA owns a 128-key tile of one (b, h) and walks the 128-row query
 // tiles that see it:
 //   warp 16    TMA producer: K, V once; per query tile Q, dO and the three
-//              256-entry distance windows (b, db/dbeta, db/dmu), 2 stages.
+//              256-entry distance windows (b, db/dbeta, db/dmu, four shifted
+//              reversed copies each for 16-byte loads), 2 stages.
 //   warp 17    MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
 //              dV += P^T dO and dK += (c dS)^T Q (A operands MN-major in shared
 //              memory, M = keys) and dQ = (c dS) K (A = c dS from TMEM).
@@ -32,6 +33,8 @@
 //              go out as bf16.
 // TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
 //               dK [384,448) dV [448,512).
+#include <type_traits>
+
 #include "table_eval.cuh"
 
 namespace bam {
@@ -44,7 +47,11 @@ constexpr int kBProducerWarp = kBCompute;
 constexpr int kBMmaWarp = kBCompute + 1;
 constexpr int kBKeysPerWarp = 128 / (kBCompute / 4);  // 32 keys of the tile per thread
 constexpr int kTile = 128 * 64 * 2;  // 16 KB bf16 tile
-constexpr int kBWin = 256;
+constexpr int kBWin = 256;            // window entries per query tile
+constexpr int kBWinCopy = kBWin + 4;  // entries per reversed copy (shifts of 0..3)
+constexpr int kBWinCopyStride = 288;
+constexpr int kBWinPlane = kTabCopies * kBWinCopyStride;
+static_assert(win_copy_off(kTabCopies - 1, kBWinCopyStride) + kBWinCopy <= kBWinPlane, "window");
 
 struct __align__(1024) BwdSmem {
   uint8_t k[kTile];
@@ -54,7 +61,7 @@ struct __align__(1024) BwdSmem {
   uint8_t pt[2 * kTile];   // P^T as an MN-major A operand: 2 atoms of 64 keys x 128 queries
   uint8_t dst[2 * kTile];  // (c dS)^T, same layout
   float dqs[2][128][32];   // dQ tile staged for the TMA reduction: two 128-B-swizzled boxes
-  float win[kBStages][3][kBWin];
+  float win[kBStages][3][kBWinPlane];  // b, db/dbeta, db/dmu: four reversed copies each
   float red[kBCompute][4];
   uint64_t kv_full;
   uint64_t dqs_full;
@@ -148,7 +155,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = sm.tmem_base;
-  const size_t plane = static_cast<size_t>(a.H) * a.tab_len;
+  const size_t copy_stride = static_cast<size_t>(a.H) * a.tab_len;  // floats between copies
+  const size_t plane = kTabCopies * copy_stride;
 
   if (warp == kBProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -173,12 +181,17 @@ __global__ void __launch_bounds__(kBThreads, 1)
           ok = mbar_wait(&sm.qd_empty[s], ((t / kBStages) - 1) & 1, a.status, ab, kSiteBProd);
           if (!ok) break;
         }
-        mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTile + 3 * kBWin * 4);
+        mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTile + 3 * kTabCopies * kBWinCopy * 4);
         tma_load_3d(sm.q[s], &tq, &sm.qd_full[s], 0, i0, bh);
         tma_load_3d(sm.dO[s], &tdo, &sm.qd_full[s], 0, i0, bh);
-        const size_t base = static_cast<size_t>(h) * a.tab_len + a.tab_off + i0 - j0 - 128;
+        // Window: table indices tab_off + i0 - j0 - 128 + [0, kBWin), which
+        // start at tab_len - kBWin minus that base in the reversed rows.
+        const float* src = a.table + static_cast<size_t>(h) * a.tab_len +
+                           (a.tab_len - kBWin - (a.tab_off + i0 - j0 - 128));
         for (int p = 0; p < 3; ++p)
-          bulk_load(sm.win[s][p], a.table + p * plane + base, kBWin * 4, &sm.qd_full[s]);
+          for (int k = 0; k < kTabCopies; ++k)
+            bulk_load(sm.win[s][p] + win_copy_off(k, kBWinCopyStride),
+                      src + p * plane + k * copy_stride, kBWinCopy * 4, &sm.qd_full[s]);
         issued = t + 1;
       }
       if (kv_issued) mbar_drain(&sm.kv_full, 0);
@@ -252,6 +265,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
     const int r = 32 * (warp & 3) + lane;  // query row within the tile = TMEM lane
     const int hc = warp >> 2;              // which 32 keys of the tile
     const uint32_t lb = tmem_lane_base(warp);
+    const int kq = (r + 1) & 3;
+    const int wrev = win_copy_off(kq, kBWinCopyStride) + (127 - r + kq);
     const float s_h = a.ssmax ? __ldg(a.s + h) : 1.0f;
     // Scalar-gradient sums as f32x2 pairs (even / odd key columns):
     // sum dS b (log2 units), sum dS db/dbeta, sum dS db/dmu, and sum over
@@ -328,7 +343,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
       const float delta = row_ok ? del_row : 0.0f;
       int lim = a.T - 1 - j0;              // last visible key column
       if (a.causal) lim = min(lim, i - j0);
-      const bool need_mask = lim < 127;
       const uint64_t cr2 = f2_pack(cr, cr), cn2 = f2_pack(cn, cn);
       const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndel2 = f2_pack(-delta, -delta);
 
@@ -337,9 +351,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
       ok = warp_wait(&sm.qd_full[s], (t / kBStages) & 1, a.status, ab, kSiteBWgQD);
       if (!ok) break;
       tc_fence_after();
-      const float* wb = sm.win[s][0] + 128 + r;
-      const float* wbeta = sm.win[s][1] + 128 + r;
-      const float* wmu = sm.win[s][2] + 128 + r;
+      // Key c of row r reads window entry 128 + r - c, i.e. reversed entry
+      // 127 - r + c; in copy kq the entries of c, c+1, c+2, c+3 (c % 4 == 0)
+      // form one aligned 16-byte vector.
+      const float* wv = sm.win[s][0] + wrev;
       // Row partial sums for the Delta correction and the SSMax sum.
       uint64_t pB2 = 0ull, pBeta2 = 0ull, pMu2 = 0ull, pS2 = 0ull, pDP2 = 0ull, rowSS2 = 0ull;
       // Four 8-key chunks of S and dP per thread.
@@ -349,42 +364,56 @@ __global__ void __launch_bounds__(kBThreads, 1)
         uint32_t sv[8], dpv[8];
         tmem_ld_32x32b_x8(tm + lb + kColS + c0, sv);
         tmem_ld_32x32b_x8(tm + lb + kColDP + c0, dpv);
+        uint64_t tb[4], tbeta[4], tmu[4];
+        const float* wp = wv + c0;
+        ld_f2x2(wp, tb[0], tb[1]);
+        ld_f2x2(wp + 4, tb[2], tb[3]);
+        ld_f2x2(wp + kBWinPlane, tbeta[0], tbeta[1]);
+        ld_f2x2(wp + kBWinPlane + 4, tbeta[2], tbeta[3]);
+        ld_f2x2(wp + 2 * kBWinPlane, tmu[0], tmu[1]);
+        ld_f2x2(wp + 2 * kBWinPlane + 4, tmu[2], tmu[3]);
         tmem_ld_wait();
         reg_fence8(sv);
         reg_fence8(dpv);
         uint32_t pp[4], dd[4];
+        // Masked keys (past the causal limit or T) only in chunks that reach
+        // them; the test is warp-uniform so each warp takes one version.
+        auto elementwise = [&](auto masked) {
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int c = c0 + 2 * x;
-          const uint64_t s2 = f2_pack(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
-          const uint64_t dp2 =
-              f2_pack(__uint_as_float(dpv[2 * x]), __uint_as_float(dpv[2 * x + 1]));
-          const uint64_t tb2 = f2_pack(wb[-c], wb[-c - 1]);
-          const uint64_t tbeta2 = f2_pack(wbeta[-c], wbeta[-c - 1]);
-          const uint64_t tmu2 = f2_pack(wmu[-c], wmu[-c - 1]);
-          float z0, z1;
-          f2_unpack(fadd2(ffma2(s2, cr2, tb2), nlse2), z0, z1);
-          if (need_mask) {
-            if (c > lim) z0 = -INFINITY;
-            if (c + 1 > lim) z1 = -INFINITY;
+          for (int x = 0; x < 4; ++x) {
+            const int c = c0 + 2 * x;
+            const uint64_t s2 =
+                f2_pack(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
+            const uint64_t dp2 =
+                f2_pack(__uint_as_float(dpv[2 * x]), __uint_as_float(dpv[2 * x + 1]));
+            float z0, z1;
+            f2_unpack(fadd2(ffma2(s2, cr2, tb[x]), nlse2), z0, z1);
+            if constexpr (decltype(masked)::value) {
+              if (c > lim) z0 = -INFINITY;
+              if (c + 1 > lim) z1 = -INFINITY;
+            }
+            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+            const uint64_t p2 = f2_pack(p0, p1);
+            const uint64_t dS2 = fmul2(p2, fadd2(dp2, ndel2));
+            accB2 = ffma2(dS2, tb[x], accB2);
+            accBeta2 = ffma2(dS2, tbeta[x], accBeta2);
+            accMu2 = ffma2(dS2, tmu[x], accMu2);
+            rowSS2 = ffma2(dS2, s2, rowSS2);
+            pB2 = ffma2(p2, tb[x], pB2);
+            pBeta2 = ffma2(p2, tbeta[x], pBeta2);
+            pMu2 = ffma2(p2, tmu[x], pMu2);
+            pS2 = ffma2(p2, s2, pS2);
+            pDP2 = ffma2(p2, dp2, pDP2);
+            pp[x] = pack_bf16x2(p0, p1);
+            float q0, q1;
+            f2_unpack(fmul2(dS2, cn2), q0, q1);
+            dd[x] = pack_bf16x2(q0, q1);
           }
-          const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-          const uint64_t p2 = f2_pack(p0, p1);
-          const uint64_t dS2 = fmul2(p2, fadd2(dp2, ndel2));
-          accB2 = ffma2(dS2, tb2, accB2);
-          accBeta2 = ffma2(dS2, tbeta2, accBeta2);
-          accMu2 = ffma2(dS2, tmu2, accMu2);
-          rowSS2 = ffma2(dS2, s2, rowSS2);
-          pB2 = ffma2(p2, tb2, pB2);
-          pBeta2 = ffma2(p2, tbeta2, pBeta2);
-          pMu2 = ffma2(p2, tmu2, pMu2);
-          pS2 = ffma2(p2, s2, pS2);
-          pDP2 = ffma2(p2, dp2, pDP2);
-          pp[x] = pack_bf16x2(p0, p1);
-          float q0, q1;
-          f2_unpack(fmul2(dS2, cn2), q0, q1);
-          dd[x] = pack_bf16x2(q0, q1);
-        }
+        };
+        if (__any_sync(0xffffffffu, c0 + 7 > lim))
+          elementwise(std::true_type{});
+        else
+          elementwise(std::false_type{});
         if (ch == 0 && t > 0) {
           // The previous tile's gradient products must be done before its
           // P^T / dS^T buffers and dS TMEM are overwritten; its dQ tile is

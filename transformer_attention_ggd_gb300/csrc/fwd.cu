@@ -13,7 +13,9 @@
 // One CTA owns 256 query rows of one (b, h) as two 128-row tiles A and B and
 // walks the key/value tiles of 128 keys:
 //   warp 8      TMA producer: Q once; per key tile K, V and the 384-entry
-//               distance window, into a 3-stage ring.
+//               distance window (four shifted reversed copies, so that a
+//               thread reads four keys' biases with one 16-byte load), into
+//               a 3-stage ring.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K^T (128x128x64, both
 //               operands K-major in shared memory) and O_t += P_t V (P from
 //               Tensor Memory, V MN-major), accumulators in Tensor Memory.
@@ -36,14 +38,18 @@ namespace {
 constexpr int kStages = 3;
 constexpr int kThreads = 320;  // 10 warps: 168 registers per thread at most
 constexpr int kTileBytes = 128 * 64 * 2;
-constexpr int kWin = 384;
+constexpr int kWin = 384;          // window entries per key tile (two query tiles)
+constexpr int kWinCopy = kWin + 4;  // entries per reversed copy (shifts of 0..3)
+constexpr int kWinCopyStride = 416;
+constexpr int kWinStage = kTabCopies * kWinCopyStride;
+static_assert(win_copy_off(kTabCopies - 1, kWinCopyStride) + kWinCopy <= kWinStage, "window");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct __align__(1024) FwdSmem {
   uint8_t q[2][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
-  float win[kStages][kWin];
+  float win[kStages][kWinStage];
   uint64_t q_full;
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
@@ -172,17 +178,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (hasB) tma_load_3d(sm.q[1], &tq, &sm.q_full, 0, i0 + 128, bh);
         q_issued = true;
       }
-      // Window of key tile j starts at d = i0 - 128 - 128 j.
-      const float* tab_h = a.table + static_cast<size_t>(h) * a.tab_len + a.tab_off + i0 - 128;
+      // The window of key tile j covers table indices tab_off + i0 - 128 -
+      // 128 j + [0, kWin); in the reversed rows it starts at tab_len - kWin
+      // minus that base (a multiple of 4 entries).
+      const size_t copy_stride = static_cast<size_t>(a.H) * a.tab_len;
+      const float* tab_h = a.table + static_cast<size_t>(h) * a.tab_len +
+                           (a.tab_len - kWin - a.tab_off - i0 + 128);
       for (int j = 0; ok && j < nKV; ++j) {
         const int s = j % kStages;
         if (j >= kStages) {
           ok = mbar_wait(&sm.kv_empty[s], ((j / kStages) - 1) & 1, a.status, ab, kSiteProducer);
           if (!ok) break;
         }
-        mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes + kWin * 4);
+        mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes + kTabCopies * kWinCopy * 4);
         tma_load_3d(sm.k[s], &tk, &sm.k_full[s], 0, 128 * j, bh);
-        bulk_load(sm.win[s], tab_h - 128 * j, kWin * 4, &sm.k_full[s]);
+        for (int k = 0; k < kTabCopies; ++k)
+          bulk_load(sm.win[s] + win_copy_off(k, kWinCopyStride), tab_h + k * copy_stride + 128 * j,
+                    kWinCopy * 4, &sm.k_full[s]);
         mbar_arrive_expect_tx(&sm.v_full[s], kTileBytes);
         tma_load_3d(sm.v[s], &tv, &sm.v_full[s], 0, 128 * j, bh);
         issued = j + 1;
@@ -272,7 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float m = -INFINITY, l = 0.0f, le = 0.0f;
     bool ok = (*ab == 0);
-    const int woff = 128 * (t + 1) + r;  // window index of column 0
+    // Column c of this row reads window entry woff - c, i.e. reversed entry
+    // kWin - 1 - woff + c; in copy kq those of c, c+1, c+2, c+3 (c % 4 == 0)
+    // form one aligned 16-byte vector.
+    const int woff = 128 * (t + 1) + r;
+    const int kq = (r + 1) & 3;
+    const int wrev = win_copy_off(kq, kWinCopyStride) + (kWin - 1 - woff + kq);
     for (int j = 0; ok && j < nt; ++j) {
       const int s = j % kStages;
       ok = warp_wait(&sm.s_full[t], j & 1, a.status, ab, kSiteSoftS);
@@ -283,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S row -> z = c_i S + bias (log2 units) as column pairs (f32x2), 32
       // columns at a time; the next chunk's TMEM load overlaps this chunk's
       // arithmetic.
-      const float* wv = sm.win[s] + woff;
+      const float* wv = sm.win[s] + wrev;
       const uint64_t cr2 = f2_pack(cr, cr);
       uint64_t z[64];
       uint32_t sr[2][16];
@@ -294,11 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ch = 0; ch < 8; ++ch) {
         if (ch < 7) tmem_ld_32x32b_x16(tS + 16 * (ch + 1), sr[(ch + 1) & 1]);
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          const int c = 16 * ch + 2 * x;
-          const uint64_t s2 = f2_pack(__uint_as_float(sr[ch & 1][2 * x]),
+        for (int x = 0; x < 8; x += 2) {
+          uint64_t t0, t1;
+          ld_f2x2(wv + 16 * ch + 2 * x, t0, t1);
+          const uint64_t s0 = f2_pack(__uint_as_float(sr[ch & 1][2 * x]),
                                       __uint_as_float(sr[ch & 1][2 * x + 1]));
-          z[8 * ch + x] = ffma2(s2, cr2, f2_pack(wv[-c], wv[-c - 1]));
+          const uint64_t s1 = f2_pack(__uint_as_float(sr[ch & 1][2 * x + 2]),
+                                      __uint_as_float(sr[ch & 1][2 * x + 3]));
+          z[8 * ch + x] = ffma2(s0, cr2, t0);
+          z[8 * ch + x + 1] = ffma2(s1, cr2, t1);
         }
         if (ch < 7) {
           tmem_ld_wait();

@@ -60,10 +60,11 @@ __device__ __forceinline__ float to_f32_finite(float f) {
 }
 
 // Entry x of head h (see TableArgs).  Shared with the backward preprocess,
-// which builds its tables in the same launch.
+// which builds its tables in the same launch.  By-distance modes write the
+// value into each reversed copy, and the thread with x < k also writes the
+// zero that pads position x of copy k.
 __device__ __forceinline__ void table_entry(const TableArgs& a, int h, int x) {
   const float alpha = a.alpha[h], beta = a.beta[h], mu = a.mu[h];
-  const size_t idx = static_cast<size_t>(h) * a.len + x;
   float b, g1, g2;
   if (a.mode == kTableDecode) {
     float val = 0.0f;
@@ -71,15 +72,22 @@ __device__ __forceinline__ void table_entry(const TableArgs& a, int h, int x) {
       bias_terms(a.Tkv - 1 - x, alpha, beta, mu, a.eps, &b, &g1, &g2);
       val = to_f32_finite(b * static_cast<float>(kLog2e));
     }
-    a.tab[idx] = val;
+    a.tab[static_cast<size_t>(h) * a.len + x] = val;
     return;
   }
   bias_terms(x - a.off, alpha, beta, mu, a.eps, &b, &g1, &g2);
-  a.tab[idx] = to_f32_finite(b * static_cast<float>(kLog2e));
-  if (a.mode == kTableBackward) {
-    const size_t plane = static_cast<size_t>(a.H) * a.len;
-    a.tab[plane + idx] = to_f32_finite(g1);
-    a.tab[2 * plane + idx] = to_f32_finite(g2);
+  const float val[3] = {to_f32_finite(b * static_cast<float>(kLog2e)), to_f32_finite(g1),
+                        to_f32_finite(g2)};
+  const int nplanes = a.mode == kTableBackward ? 3 : 1;
+  const size_t row = static_cast<size_t>(a.len);
+  const size_t plane = static_cast<size_t>(kTabCopies) * a.H * row;
+  for (int p = 0; p < nplanes; ++p) {
+#pragma unroll
+    for (int k = 0; k < kTabCopies; ++k) {
+      float* dst = a.tab + p * plane + (static_cast<size_t>(k) * a.H + h) * row;
+      if (x >= k) dst[a.len - 1 - x + k] = val[p];
+      if (x < k) dst[x] = 0.0f;
+    }
   }
 }
 
