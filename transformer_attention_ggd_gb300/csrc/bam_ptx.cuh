@@ -74,6 +74,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware until the phase
+// completes or about `hint_ns` nanoseconds have passed, instead of returning
+// at once: a waiting warp then issues almost nothing.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Device status words shared by every CTA of a launch (in the caller's workspace).
 struct DevStatus {
   int abort;      // nonzero: some thread gave up; everyone else leaves early
@@ -86,6 +101,9 @@ enum : int { BAM_DEV_OK = 0, BAM_DEV_TIMEOUT = 1, BAM_DEV_ABORTED = 2 };
 
 // Wall-clock budget of one wait.  Normal waits last microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Longest hardware sleep of one try in the slow path: short enough that the
+// abort words and the wall clock are still checked often.
+constexpr uint32_t kWaitSleepNs = 20000;  // 20 us
 
 __device__ __forceinline__ void raise_abort(DevStatus* st, volatile int* cta_abort, int site) {
   *cta_abort = 1;
@@ -101,8 +119,8 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
                                             volatile int* cta_abort, int site) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if ((it & 3u) == 0) {
       if (*cta_abort) return false;
       if (*reinterpret_cast<volatile int*>(&st->abort)) {
         *cta_abort = 1;
@@ -339,6 +357,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// lo_acc += low bf16 half of w, hi_acc += high half: the widening to fp32 is
+// exact, so this equals adding the unpacked values (sm_100+ mixed-type add).
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t w, float& lo_acc, float& hi_acc) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n add.rn.f32.bf16 %0, l, %0;\n"
+      " add.rn.f32.bf16 %1, h, %1;\n}\n"
+      : "+f"(lo_acc), "+f"(hi_acc)
+      : "r"(w));
 }
 
 // Packed pairs of fp32 values in one 64-bit register pair (sm_100+ f32x2 ops).

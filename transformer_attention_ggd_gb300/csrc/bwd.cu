@@ -24,13 +24,16 @@
 //   warp 17    MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
 //              dV += P^T dO and dK += (c dS)^T Q (A operands MN-major in shared
 //              memory, M = keys) and dQ = (c dS) K (A = c dS from TMEM).
+//              S and dP of the next query tile are issued as soon as every
+//              element-wise warp has read its last S/dP columns of this one,
+//              so they overlap the end of this tile's element-wise work.
 //   warps 0-15 four warps per TMEM lane quarter; each thread owns one query
 //              row and one quarter (32 keys) of the tile: P, dS, the scalar-
 //              gradient sums (as f32x2 pairs of partial sums), P and c*dS to
 //              shared memory and c*dS to TMEM; the finished dQ tile goes
 //              through a shared staging tile into the fp32 accumulator with
-//              TMA reductions.  At the end, dK and dV rows (TMEM lane = key)
-//              go out as bf16.
+//              TMA reductions, which run in the background.  At the end, dK
+//              and dV rows (TMEM lane = key) go out as bf16.
 // TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
 //               dK [384,448) dV [448,512).
 #include <type_traits>
@@ -69,6 +72,7 @@ struct __align__(1024) BwdSmem {
   uint64_t qd_full[kBStages];
   uint64_t qd_empty[kBStages];
   uint64_t s_full;
+  uint64_t sdp_free;
   uint64_t ds_ready;
   uint64_t mma_done;
   uint64_t mma_final;
@@ -81,6 +85,7 @@ enum : int {
   kSiteBMmaKV = 60,
   kSiteBMmaQD = 61,
   kSiteBMmaDS = 62,
+  kSiteBMmaFree = 63,
   kSiteBWgS = 70,
   kSiteBWgQD = 71,
   kSiteBWgDone = 72,
@@ -115,9 +120,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
     bam_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  BwdSmem& sm = *reinterpret_cast<BwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  // Aligned by an offset from the shared array itself (not through an
+  // integer cast), so that accesses stay in the shared address space.
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw + ((0u - smem_u32(smem_raw)) & 1023u));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int BH = a.B * a.H;
@@ -140,6 +146,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       mbar_init(&sm.qd_empty[s], 1);
     }
     mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.sdp_free, kBCompute);
     mbar_init(&sm.ds_ready, kBCompute);
     mbar_init(&sm.dqs_full, kBCompute);
     mbar_init(&sm.dqs_free, 1);
@@ -227,20 +234,19 @@ __global__ void __launch_bounds__(kBThreads, 1)
       }
       for (int t = 0; ok && t < nq; ++t) {
         const int s = t % kBStages;
-        ok = mbar_wait(&sm.ds_ready, t & 1, a.status, ab, kSiteBMmaDS);
-        if (!ok) break;
-        tc_fence_after();
-        // S and dP of the next tile first: their TMEM was read by the
-        // element-wise warps before ds_ready, and issuing them ahead of this
-        // tile's three gradient products lets the next tile's element-wise
-        // work overlap those products.
+        // S and dP of the next tile once this tile's S/dP columns are read.
         if (t + 1 < nq) {
+          ok = mbar_wait(&sm.sdp_free, t & 1, a.status, ab, kSiteBMmaFree);
+          if (!ok) break;
           ok = mbar_wait(&sm.qd_full[(t + 1) % kBStages], ((t + 1) / kBStages) & 1, a.status, ab,
                          kSiteBMmaQD);
           if (!ok) break;
           tc_fence_after();
           issue_s_dp((t + 1) % kBStages);
         }
+        ok = mbar_wait(&sm.ds_ready, t & 1, a.status, ab, kSiteBMmaDS);
+        if (!ok) break;
+        tc_fence_after();
         const uint32_t qa = smem_u32(sm.q[s]), da = smem_u32(sm.dO[s]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
@@ -275,12 +281,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
     float acc_s = 0.f;
     bool ok = (*ab == 0);
     // dQ of a finished query tile: TMEM -> shared staging tile -> one TMA
-    // reduction (add) per 32-column box into the fp32 accumulator.  Rows past
-    // T are clipped by the tensor map.  Hand-offs use bounded mbarrier waits
-    // (never a hardware barrier), so that a warp that gives up cannot leave the
-    // others blocked: thread 0 releases the staging tile once the previous
-    // reduction has read it (dqs_free), every warp arrives once its part is
-    // written (dqs_full), and thread 0 then issues the reduction.
+    // reduction (add) per 32-column box into the fp32 accumulator; the
+    // reduction runs in the background.  Rows past T are clipped by the
+    // tensor map.  Hand-offs use bounded mbarrier waits (never a hardware
+    // barrier), so that a warp that gives up cannot leave the others
+    // blocked: thread 0 releases the staging tile once the previous reduction
+    // has read it (dqs_free), every warp arrives once its part is written
+    // (dqs_full), and thread 0 then issues the reduction.
     int n_dq = 0;  // dQ tiles staged so far
     auto dq_epilogue = [&](int t) -> bool {
       uint32_t dv[16];
@@ -375,6 +382,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
         tmem_ld_wait();
         reg_fence8(sv);
         reg_fence8(dpv);
+        if (ch == 3) {
+          // This warp's last S/dP columns of the tile are in registers: the
+          // next tile's S and dP may be written over them.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.sdp_free);
+        }
         uint32_t pp[4], dd[4];
         // Masked keys (past the causal limit or T) only in chunks that reach
         // them; the test is warp-uniform so each warp takes one version.

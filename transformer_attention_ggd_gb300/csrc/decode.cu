@@ -65,9 +65,10 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float* o, float 
 
 __global__ void __launch_bounds__(kDecThreads)
     bam_decode_kernel(const DecodeArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  DecSmem& sm = *reinterpret_cast<DecSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                            ~static_cast<uintptr_t>(127));
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  // Aligned by an offset from the shared array itself (not through an
+  // integer cast), so that accesses stay in the shared address space.
+  DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw + ((0u - smem_u32(smem_raw)) & 127u));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int sp = blockIdx.x;

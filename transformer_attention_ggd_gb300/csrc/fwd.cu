@@ -113,9 +113,10 @@ __device__ __forceinline__ void store_row(const FwdArgs& a, int64_t row, const u
 __global__ void __launch_bounds__(kThreads, 1)
     bam_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  // Aligned by an offset from the shared array itself (not through an
+  // integer cast), so that accesses stay in the shared address space.
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(smem_raw + ((0u - smem_u32(smem_raw)) & 1023u));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -297,33 +298,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&sm.k_full[s], (j / kStages) & 1, a.status, ab, kSiteSoftK);
       if (!ok) break;
       tc_fence_after();
-      // S row -> z = c_i S + bias (log2 units) as column pairs (f32x2), 32
+      // S row -> z = c_i S + bias (log2 units) as column pairs (f32x2), 8
       // columns at a time; the next chunk's TMEM load overlaps this chunk's
       // arithmetic.
       const float* wv = sm.win[s] + wrev;
       const uint64_t cr2 = f2_pack(cr, cr);
       uint64_t z[64];
-      uint32_t sr[2][16];
-      tmem_ld_32x32b_x16(tS, sr[0]);
+      uint32_t sr[2][8];
+      tmem_ld_32x32b_x8(tS, sr[0]);
       tmem_ld_wait();
-      reg_fence16(sr[0]);
+      reg_fence8(sr[0]);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        if (ch < 7) tmem_ld_32x32b_x16(tS + 16 * (ch + 1), sr[(ch + 1) & 1]);
+      for (int ch = 0; ch < 16; ++ch) {
+        if (ch < 15) tmem_ld_32x32b_x8(tS + 8 * (ch + 1), sr[(ch + 1) & 1]);
 #pragma unroll
-        for (int x = 0; x < 8; x += 2) {
+        for (int x = 0; x < 4; x += 2) {
           uint64_t t0, t1;
-          ld_f2x2(wv + 16 * ch + 2 * x, t0, t1);
+          ld_f2x2(wv + 8 * ch + 2 * x, t0, t1);
           const uint64_t s0 = f2_pack(__uint_as_float(sr[ch & 1][2 * x]),
                                       __uint_as_float(sr[ch & 1][2 * x + 1]));
           const uint64_t s1 = f2_pack(__uint_as_float(sr[ch & 1][2 * x + 2]),
                                       __uint_as_float(sr[ch & 1][2 * x + 3]));
-          z[8 * ch + x] = ffma2(s0, cr2, t0);
-          z[8 * ch + x + 1] = ffma2(s1, cr2, t1);
+          z[4 * ch + x] = ffma2(s0, cr2, t0);
+          z[4 * ch + x + 1] = ffma2(s1, cr2, t1);
         }
-        if (ch < 7) {
+        if (ch < 15) {
           tmem_ld_wait();
-          reg_fence16(sr[(ch + 1) & 1]);
+          reg_fence8(sr[(ch + 1) & 1]);
         }
       }
       tc_fence_before();
@@ -379,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // columns at a time, and the two row sums (rounded weights for O,
       // unrounded for the LSE) in independent partial sums.
       const uint64_t negm2 = f2_pack(-m, -m);
-      uint64_t lr2[2] = {0ull, 0ull}, le2[2] = {0ull, 0ull};
+      float lr[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t le2[2] = {0ull, 0ull};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
@@ -392,17 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p1 = ex2_approx(a1);
           const uint32_t w = pack_bf16x2(p0, p1);
           pk[y] = w;
-          lr2[y & 1] = fadd2(lr2[y & 1], f2_pack(__uint_as_float(w << 16),
-                                                 __uint_as_float(w & 0xFFFF0000u)));
+          add_bf16x2_f32(w, lr[2 * (y & 1)], lr[2 * (y & 1) + 1]);
           le2[y & 1] = fadd2(le2[y & 1], f2_pack(p0, p1));
         }
         tmem_st_32x32b_x16(tP + 16 * q, pk);
       }
       {
-        float a0, a1, b0, b1;
-        f2_unpack(fadd2(lr2[0], lr2[1]), a0, a1);
+        float b0, b1;
         f2_unpack(fadd2(le2[0], le2[1]), b0, b1);
-        l += a0 + a1;
+        l += (lr[0] + lr[1]) + (lr[2] + lr[3]);
         le += b0 + b1;
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
