@@ -27,13 +27,16 @@
 //              S and dP of the next query tile are issued as soon as every
 //              element-wise warp has read its last S/dP columns of this one,
 //              so they overlap the end of this tile's element-wise work.
+//   warp 18    dQ reducer: issues the TMA reduction of each staged dQ tile
+//              into the fp32 accumulator and frees the staging tile.
 //   warps 0-15 four warps per TMEM lane quarter; each thread owns one query
 //              row and one quarter (32 keys) of the tile: P, dS, the scalar-
 //              gradient sums (as f32x2 pairs of partial sums), P and c*dS to
-//              shared memory and c*dS to TMEM; the finished dQ tile goes
-//              through a shared staging tile into the fp32 accumulator with
-//              TMA reductions, which run in the background.  At the end, dK
-//              and dV rows (TMEM lane = key) go out as bf16.
+//              shared memory and c*dS to TMEM (each chunk stored one chunk
+//              later, so the wait for the previous tile's products overlaps
+//              arithmetic); the finished dQ tile goes to a shared staging
+//              tile for warp 18.  At the end, dK and dV rows (TMEM lane =
+//              key) go out as bf16.
 // TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
 //               dK [384,448) dV [448,512).
 #include <type_traits>
@@ -45,9 +48,12 @@ namespace {
 
 constexpr int kBStages = 2;
 constexpr int kBCompute = 16;   // element-wise warps: four per TMEM lane quarter
-constexpr int kBThreads = 32 * (kBCompute + 2);  // + producer + MMA issuer
+// + producer + MMA issuer + dQ reducer (still 96 registers per thread: the
+// register file is split per scheduler, and 19 warps put at most 5 on one)
+constexpr int kBThreads = 32 * (kBCompute + 3);
 constexpr int kBProducerWarp = kBCompute;
 constexpr int kBMmaWarp = kBCompute + 1;
+constexpr int kBDqWarp = kBCompute + 2;
 constexpr int kBKeysPerWarp = 128 / (kBCompute / 4);  // 32 keys of the tile per thread
 constexpr int kTile = 128 * 64 * 2;  // 16 KB bf16 tile
 constexpr int kBWin = 256;            // window entries per query tile
@@ -86,6 +92,7 @@ enum : int {
   kSiteBMmaQD = 61,
   kSiteBMmaDS = 62,
   kSiteBMmaFree = 63,
+  kSiteBDq = 64,
   kSiteBWgS = 70,
   kSiteBWgQD = 71,
   kSiteBWgDone = 72,
@@ -266,6 +273,24 @@ __global__ void __launch_bounds__(kBThreads, 1)
       umma_commit(&sm.mma_final);
       mbar_drain(&sm.mma_final, 0);
     }
+  } else if (warp == kBDqWarp) {
+    // ------------------------------------------------------------ dQ reducer
+    if (lane == 0) {
+      bool ok = (*ab == 0);
+      for (int t = 0; ok && t < nq; ++t) {
+        ok = mbar_wait(&sm.dqs_full, t & 1, a.status, ab, kSiteBDq);
+        if (!ok) break;
+        const int i0 = (q_first + t) * 128;
+        tma_reduce_add_3d(&tdq, sm.dqs[0], 0, i0, bh);
+        tma_reduce_add_3d(&tdq, sm.dqs[1], 32, i0, bh);
+        bulk_commit();
+        bulk_wait_read_all();  // staging tile read: it may be written again
+        mbar_arrive(&sm.dqs_free);
+      }
+      // The staging tile must stay valid until the last reduction has read
+      // it; the writes themselves complete with the grid.
+      bulk_wait_read_all();
+    }
   } else {
     // ------------------------------------------------------------ element-wise
     const int r = 32 * (warp & 3) + lane;  // query row within the tile = TMEM lane
@@ -280,27 +305,19 @@ __global__ void __launch_bounds__(kBThreads, 1)
     uint64_t accB2 = 0ull, accBeta2 = 0ull, accMu2 = 0ull;
     float acc_s = 0.f;
     bool ok = (*ab == 0);
-    // dQ of a finished query tile: TMEM -> shared staging tile -> one TMA
-    // reduction (add) per 32-column box into the fp32 accumulator; the
-    // reduction runs in the background.  Rows past T are clipped by the
-    // tensor map.  Hand-offs use bounded mbarrier waits (never a hardware
-    // barrier), so that a warp that gives up cannot leave the others
-    // blocked: thread 0 releases the staging tile once the previous reduction
-    // has read it (dqs_free), every warp arrives once its part is written
-    // (dqs_full), and thread 0 then issues the reduction.
+    // dQ of a finished query tile: TMEM -> shared staging tile (two
+    // 128-byte-swizzled 32-column boxes) for the dQ warp's TMA reductions.
+    // Hand-offs use bounded mbarrier waits: the staging tile is written once
+    // the dQ warp has seen the previous reduction read it (dqs_free), and
+    // every warp arrives on dqs_full when its part is written.
     int n_dq = 0;  // dQ tiles staged so far
-    auto dq_epilogue = [&](int t) -> bool {
+    auto dq_epilogue = [&]() -> bool {
       uint32_t dv[16];
       tmem_ld_32x32b_x16(tm + lb + kColDQ + 16 * hc, dv);
       tmem_ld_wait();
       reg_fence16(dv);
-      if (n_dq > 0) {
-        if (threadIdx.x == 0) {
-          bulk_wait_read_all();
-          mbar_arrive(&sm.dqs_free);
-        }
-        if (!warp_wait(&sm.dqs_free, (n_dq - 1) & 1, a.status, ab, kSiteBWgDq)) return false;
-      }
+      if (n_dq > 0 && !warp_wait(&sm.dqs_free, (n_dq - 1) & 1, a.status, ab, kSiteBWgDq))
+        return false;
       uint8_t* box = reinterpret_cast<uint8_t*>(sm.dqs[hc >> 1]);
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
@@ -311,13 +328,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.dqs_full);
-      if (threadIdx.x == 0) {
-        if (!mbar_wait(&sm.dqs_full, n_dq & 1, a.status, ab, kSiteBWgDq)) return false;
-        const int i0 = (q_first + t) * 128;
-        tma_reduce_add_3d(&tdq, sm.dqs[0], 0, i0, bh);
-        tma_reduce_add_3d(&tdq, sm.dqs[1], 32, i0, bh);
-        bulk_commit();
-      }
       ++n_dq;
       return true;
     };
@@ -364,6 +374,15 @@ __global__ void __launch_bounds__(kBThreads, 1)
       const float* wv = sm.win[s][0] + wrev;
       // Row partial sums for the Delta correction and the SSMax sum.
       uint64_t pB2 = 0ull, pBeta2 = 0ull, pMu2 = 0ull, pS2 = 0ull, pDP2 = 0ull, rowSS2 = 0ull;
+      // P and c*dS of keys [c0, c0+8) of query row r into the MN-major
+      // operands (one 16-byte chunk each) and c*dS into TMEM.
+      auto store_chunk = [&](int c0, const uint32_t* pp, const uint32_t* dd) {
+        const uint32_t off = mn_chunk_offset(c0 / 8, r);
+        *reinterpret_cast<uint4*>(sm.pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+        *reinterpret_cast<uint4*>(sm.dst + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+        tmem_st_32x32b_x4(tm + lb + kColDS + c0 / 2, dd);
+      };
+      uint32_t pp_prev[4], dd_prev[4];  // chunk computed, not yet stored
       // Four 8-key chunks of S and dP per thread.
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
@@ -428,27 +447,27 @@ __global__ void __launch_bounds__(kBThreads, 1)
           elementwise(std::true_type{});
         else
           elementwise(std::false_type{});
-        if (ch == 0 && t > 0) {
+        if (ch == 1 && t > 0) {
           // The previous tile's gradient products must be done before its
           // P^T / dS^T buffers and dS TMEM are overwritten; its dQ tile is
           // drained here, before this tile's dQ product is issued.
           ok = warp_wait(&sm.mma_done, (t - 1) & 1, a.status, ab, kSiteBWgDone);
           if (!ok) break;
           tc_fence_after();
-          if (!dq_epilogue(t - 1)) {
+          if (!dq_epilogue()) {
             ok = false;
             break;
           }
         }
-        // P and c*dS, keys [c0, c0+8) of query row r, into the MN-major
-        // operands (one 16-byte chunk each) and c*dS into TMEM.
-        {
-          const uint32_t off = mn_chunk_offset(c0 / 8, r);
-          *reinterpret_cast<uint4*>(sm.pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
-          *reinterpret_cast<uint4*>(sm.dst + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+        if (ch > 0) store_chunk(c0 - 8, pp_prev, dd_prev);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          pp_prev[x] = pp[x];
+          dd_prev[x] = dd[x];
         }
-        tmem_st_32x32b_x4(tm + lb + kColDS + c0 / 2, dd);
       }
+      if (!ok) break;
+      store_chunk(kBKeysPerWarp * hc + 24, pp_prev, dd_prev);
       if (!ok) break;
       {
         float a0, a1;
@@ -472,11 +491,36 @@ __global__ void __launch_bounds__(kBThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.ds_ready);
     }
+    // Block reduction of the scalar-gradient sums, one atomic per head and sum
+    // (while the last tile's gradient products run).
+    float v4[4];
+    {
+      float a0, a1;
+      f2_unpack(accB2, a0, a1);
+      v4[0] = a0 + a1;
+      f2_unpack(accBeta2, a0, a1);
+      v4[1] = a0 + a1;
+      f2_unpack(accMu2, a0, a1);
+      v4[2] = a0 + a1;
+      v4[3] = acc_s;
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v4[x] += __shfl_xor_sync(0xffffffffu, v4[x], off);
+    if (lane == 0)
+      for (int x = 0; x < 4; ++x) sm.red[warp][x] = v4[x];
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kBCompute) : "memory");
+    if (threadIdx.x < 4 && ok) {
+      float tot = 0.f;
+      for (int w = 0; w < kBCompute; ++w) tot += sm.red[w][threadIdx.x];
+      atomicAdd(a.gacc + threadIdx.x * a.H + h, tot);
+    }
     if (ok && nq > 0) {
       ok = warp_wait(&sm.mma_done, (nq - 1) & 1, a.status, ab, kSiteBWgDone);
       if (ok) {
         tc_fence_after();
-        ok = dq_epilogue(nq - 1);
+        ok = dq_epilogue();
       }
       if (ok) {
         // dK and dV rows: TMEM lane = key j0 + r; this warp writes 16 of the
@@ -502,31 +546,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
           }
         }
       }
-    }
-    if (threadIdx.x == 0) bulk_wait_all();  // dQ reductions complete before exit
-    // Block reduction of the scalar-gradient sums, one atomic per head and sum.
-    float v4[4];
-    {
-      float a0, a1;
-      f2_unpack(accB2, a0, a1);
-      v4[0] = a0 + a1;
-      f2_unpack(accBeta2, a0, a1);
-      v4[1] = a0 + a1;
-      f2_unpack(accMu2, a0, a1);
-      v4[2] = a0 + a1;
-      v4[3] = acc_s;
-    }
-#pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v4[x] += __shfl_xor_sync(0xffffffffu, v4[x], off);
-    if (lane == 0)
-      for (int x = 0; x < 4; ++x) sm.red[warp][x] = v4[x];
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kBCompute) : "memory");
-    if (threadIdx.x < 4 && ok) {
-      float tot = 0.f;
-      for (int w = 0; w < kBCompute; ++w) tot += sm.red[w][threadIdx.x];
-      atomicAdd(a.gacc + threadIdx.x * a.H + h, tot);
     }
   }
 
