@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(256) bam_bwd_prep_kernel(const BwdArgs a, int 
 // dq (bf16) from the fp32 accumulator; the Delta correction of the scalar
 // sums (row blocks of one (b, h) per CTA); the last CTA writes the per-head
 // scalar gradients.
-constexpr int kFinalRows = 2048;
+constexpr int kFinalRows = 256;
 
 __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
   grid_dep_wait();  // dq accumulator, row sums and scalar sums of the fused kernel
@@ -629,10 +629,24 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
   if (*reinterpret_cast<volatile int*>(&a.status->abort)) return;
   const float4* src = reinterpret_cast<const float4*>(a.dq_acc);
   uint4* dst = reinterpret_cast<uint4*>(a.dq);
-  for (size_t x = tid; x < n8; x += nthreads) {
-    const float4 u = src[2 * x], w = src[2 * x + 1];
-    dst[x] = make_uint4(pack_bf16x2(u.x, u.y), pack_bf16x2(u.z, u.w), pack_bf16x2(w.x, w.y),
-                        pack_bf16x2(w.z, w.w));
+  // Four groups of eight values per thread and pass, all loads issued first.
+  for (size_t x0 = tid; x0 < n8; x0 += 4 * nthreads) {
+    float4 u[4], w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const size_t x = x0 + k * nthreads;
+      if (x < n8) {
+        u[k] = __ldcs(src + 2 * x);
+        w[k] = __ldcs(src + 2 * x + 1);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const size_t x = x0 + k * nthreads;
+      if (x < n8)
+        dst[x] = make_uint4(pack_bf16x2(u[k].x, u[k].y), pack_bf16x2(u[k].z, u[k].w),
+                            pack_bf16x2(w[k].x, w[k].y), pack_bf16x2(w[k].z, w[k].w));
+    }
   }
   // Correction sum_i (Delta_i - C_i) B_i over this CTA's rows.
   const int chunks = (a.T + kFinalRows - 1) / kFinalRows;
@@ -690,7 +704,7 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st) {
   const size_t rows = static_cast<size_t>(a.B) * a.H * a.T;
   size_t want = (rows * 8 + 255) / 256;
   if (want < 1) want = 1;
-  if (want > 152 * 4) want = 152 * 4;
+  if (want > 152 * 7) want = 152 * 7;
   const size_t tab_entries = static_cast<size_t>(a.tab.H) * a.tab.len;
   size_t tb = (tab_entries + 255) / 256;
   if (tb > 152 * 2) tb = 152 * 2;
@@ -719,9 +733,11 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
   const size_t n8 = static_cast<size_t>(a.B) * a.H * a.T * (kHeadDim / 8);
   const size_t items = static_cast<size_t>(a.B) * a.H * ((a.T + kFinalRows - 1) / kFinalRows);
-  size_t want = (n8 + 255) / 256;
+  // Enough threads that each converts about four groups; up to eight
+  // 256-thread CTAs per SM.
+  size_t want = (n8 + 1023) / 1024;
   if (want < items) want = items;
-  if (want > 152 * 2) want = 152 * 2;
+  if (want > 152 * 8) want = 152 * 8;
   const unsigned grid = static_cast<unsigned>(want);
   return launch_k(bam_bwd_final_kernel, dim3(grid), dim3(256), 0, st, true, a);
 }

@@ -213,21 +213,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = (*ab == 0);
       const uint32_t idS = idesc_bf16(128, 128, false, false);
       const uint32_t idO = idesc_bf16(128, 64, false, true);
+      // Shared-memory descriptors of the first Q, K and V tiles; the others
+      // (and the K-steps inside a tile) are fixed offsets from them, so each
+      // MMA costs the issuing thread only an add or two.
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), 16384, 1024);
+      constexpr uint64_t kTileDesc = kTileBytes >> 4;  // descriptor units of 16 bytes
       auto issue_S = [&](int t, int s) {
-        const uint32_t qa = smem_u32(sm.q[t]);
-        const uint32_t ka = smem_u32(sm.k[s]);
+        const uint64_t qd = dq0 + kTileDesc * t, kd = dk0 + kTileDesc * s;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_ss(tm + 128 * t, sdesc_sw128(qa + 32 * kk, 16, 1024),
-                  sdesc_sw128(ka + 32 * kk, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          umma_ss(tm + 128 * t, qd + 2 * kk, kd + 2 * kk, idS, kk > 0 ? 1u : 0u);
         umma_commit(&sm.s_full[t]);
       };
       auto issue_PV = [&](int t, int s, int j) {
-        const uint32_t va = smem_u32(sm.v[s]);
+        const uint64_t vd = dv0 + kTileDesc * s;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tm + 384 + 64 * t, tm + 256 + 64 * t + 8 * kk,
-                  sdesc_sw128(va + 2048 * kk, 16384, 1024), idO, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tm + 384 + 64 * t, tm + 256 + 64 * t + 8 * kk, vd + 128 * kk, idO,
+                  (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&sm.pv_done[t]);
       };
       if (ok) ok = mbar_wait(&sm.q_full, 0, a.status, ab, kSiteMmaQ);
@@ -246,14 +251,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = mbar_wait(&sm.v_full[s], (j / kStages) & 1, a.status, ab, kSiteMmaV);
         if (!ok) break;
+        // Per query tile: S of the next key tile once the softmax has copied
+        // the current S row, then PV once the probabilities are in, tile A's
+        // pair before tile B's.  That order delays tile B by about half a
+        // key tile at the start, after which the two softmax groups run
+        // staggered (measured faster on long rows).  With only a few key
+        // tiles the delay is not repaid, so there tile B's second S is
+        // issued together with tile A's.
+        const bool early_b = (j == 0 && nKV <= 8 && nB > 1);
         for (int t = 0; t < 2 && ok; ++t) {
           const int nt = t ? nB : nA;
           if (j >= nt) continue;
-          if (j + 1 < nt) {
+          if (j + 1 < nt && !(early_b && t == 1)) {
             ok = mbar_wait(&sm.s_free[t], j & 1, a.status, ab, kSiteMmaSFree);
             if (!ok) break;
             tc_fence_after();
             issue_S(t, (j + 1) % kStages);
+          }
+          if (early_b && t == 0) {
+            ok = mbar_wait(&sm.s_free[1], 0, a.status, ab, kSiteMmaSFree);
+            if (!ok) break;
+            tc_fence_after();
+            issue_S(1, 1 % kStages);
           }
           ok = mbar_wait(&sm.p_full[t], j & 1, a.status, ab, kSiteMmaP);
           if (!ok) break;
