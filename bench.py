@@ -477,6 +477,54 @@ def run_reference(args):
     }
 
 
+PROFILE_CASES = ("train", "prefill32k", "prefill262k", "decode")
+
+
+def profile_case(name, warmup):
+    """A few untimed calls of one workload, for capturing its kernels with a
+    profiler (no JSON line)."""
+    import torch
+    import __graft_entry__
+    from transformer_attention_ggd_gb300 import bam_attn as ba
+    from transformer_attention_ggd_gb300.inputs import make_inputs
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = {"train": 2, "prefill32k": 3, "prefill262k": 4, "decode": 5}[name]
+    d = make_inputs(cfg)
+
+    def bf(b):
+        return torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    p = {n: torch.from_numpy(d[n]).to(dev) for n in ("alpha", "beta", "mu", "s")}
+    prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, True, True)
+    B, H, T = d["B"], d["H"], d["T"]
+    q, k, v = bf(d["q"]), bf(d["k"]), bf(d["v"])
+    for _ in range(warmup + 1):
+        if name == "decode":
+            o = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+            ws = ba.workspace(ba.BAM_OP_DECODE, B, H, T, dev)
+            ba.bam_attn_decode(q, k, v, o, lse, prm, ws)
+        elif name == "train":
+            o = torch.empty((B, H, T, D), dtype=torch.float32, device=dev)
+            lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+            wf = ba.workspace(ba.BAM_OP_FWD, B, H, T, dev)
+            wb = ba.workspace(ba.BAM_OP_BWD, B, H, T, dev)
+            do = bf(d["do"])
+            dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+            g = [torch.empty(H, dtype=torch.float32, device=dev) for _ in range(4)]
+            ba.bam_attn_fwd(q, k, v, o, lse, prm, wf)
+            ba.bam_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, *g, prm, wb)
+        else:
+            o = torch.empty((B, H, T, D), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+            ws = ba.workspace(ba.BAM_OP_FWD, B, H, T, dev)
+            ba.bam_attn_fwd(q, k, v, o, lse, prm, ws)
+    torch.cuda.synchronize()
+    print(f"profile case {name}: {warmup + 1} calls, {ba.bam_attn_launch_count()} launches")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -485,9 +533,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip prefill/decode extras")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="only run a few untimed calls of one workload (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.profile_case:
+        profile_case(args.profile_case, args.warmup)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -219,18 +219,27 @@ __global__ void __launch_bounds__(kBThreads, 1)
       const uint32_t idSP = idesc_bf16(128, 128, false, false);
       const uint32_t idKV = idesc_bf16(128, 64, true, true);
       const uint32_t idQ = idesc_bf16(128, 64, false, true);
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
-      const uint32_t pta = smem_u32(sm.pt), dsa = smem_u32(sm.dst);
+      // Shared-memory descriptors: K-major views (S, dP) and MN-major views
+      // (the gradient products) of the tiles; stages and K-steps are fixed
+      // offsets (16-byte units) from these, so each MMA costs an add or two.
+      constexpr uint64_t kTileDesc = kTile >> 4;
+      const uint64_t qK0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sm.dO[0]), 16, 1024);
+      const uint64_t kK = sdesc_sw128(smem_u32(sm.k), 16, 1024);
+      const uint64_t vK = sdesc_sw128(smem_u32(sm.v), 16, 1024);
+      const uint64_t qM0 = sdesc_sw128(smem_u32(sm.q[0]), kTile, 1024);
+      const uint64_t dM0 = sdesc_sw128(smem_u32(sm.dO[0]), kTile, 1024);
+      const uint64_t kM = sdesc_sw128(smem_u32(sm.k), kTile, 1024);
+      const uint64_t ptM = sdesc_sw128(smem_u32(sm.pt), kTile, 1024);
+      const uint64_t dsM = sdesc_sw128(smem_u32(sm.dst), kTile, 1024);
       auto issue_s_dp = [&](int s) {
-        const uint32_t qa = smem_u32(sm.q[s]), da = smem_u32(sm.dO[s]);
+        const uint64_t qd = qK0 + kTileDesc * s, dd = dK0 + kTileDesc * s;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_ss(tm + kColS, sdesc_sw128(qa + 32 * kk, 16, 1024),
-                  sdesc_sw128(ka + 32 * kk, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+          umma_ss(tm + kColS, qd + 2 * kk, kK + 2 * kk, idSP, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_ss(tm + kColDP, sdesc_sw128(da + 32 * kk, 16, 1024),
-                  sdesc_sw128(va + 32 * kk, 16, 1024), idSP, kk > 0 ? 1u : 0u);
+          umma_ss(tm + kColDP, dd + 2 * kk, vK + 2 * kk, idSP, kk > 0 ? 1u : 0u);
         umma_commit(&sm.s_full);
       };
       if (ok) ok = mbar_wait(&sm.kv_full, 0, a.status, ab, kSiteBMmaKV);
@@ -254,19 +263,16 @@ __global__ void __launch_bounds__(kBThreads, 1)
         ok = mbar_wait(&sm.ds_ready, t & 1, a.status, ab, kSiteBMmaDS);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t qa = smem_u32(sm.q[s]), da = smem_u32(sm.dO[s]);
+        const uint64_t qd = qM0 + kTileDesc * s, dd = dM0 + kTileDesc * s;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
-          umma_ss(tm + kColDV, sdesc_sw128(pta + 2048 * kk, kTile, 1024),
-                  sdesc_sw128(da + 2048 * kk, kTile, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_ss(tm + kColDV, ptM + 128 * kk, dd + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dK += (c dS)^T Q
-          umma_ss(tm + kColDK, sdesc_sw128(dsa + 2048 * kk, kTile, 1024),
-                  sdesc_sw128(qa + 2048 * kk, kTile, 1024), idKV, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_ss(tm + kColDK, dsM + 128 * kk, qd + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dQ = (c dS) K
-          umma_ts(tm + kColDQ, tm + kColDS + 8 * kk, sdesc_sw128(ka + 2048 * kk, kTile, 1024),
-                  idQ, kk > 0 ? 1u : 0u);
+          umma_ts(tm + kColDQ, tm + kColDS + 8 * kk, kM + 128 * kk, idQ, kk > 0 ? 1u : 0u);
         umma_commit(&sm.mma_done);
         umma_commit(&sm.qd_empty[s]);
       }
