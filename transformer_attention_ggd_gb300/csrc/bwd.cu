@@ -144,9 +144,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    // Tables, Delta and the zeroed accumulators come from the preprocess.
-    grid_dep_wait();
-    sm.abort_flag = *reinterpret_cast<volatile int*>(&a.status->abort);
+    sm.abort_flag = 0;
     mbar_init(&sm.kv_full, 1);
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(&sm.qd_full[s], 1);
@@ -168,6 +166,11 @@ __global__ void __launch_bounds__(kBThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Tables, Delta, the zeroed accumulators and the cleared status word come
+  // from the preprocess.  Only the producer runs ahead of it (its K, V, Q
+  // and dO loads need nothing from it); every other thread waits here,
+  // before its first look at the status word.
+  if (warp != kBProducerWarp) grid_dep_wait();
   const uint32_t tm = sm.tmem_base;
   const size_t copy_stride = static_cast<size_t>(a.H) * a.tab_len;  // floats between copies
   const size_t plane = kTabCopies * copy_stride;
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTile + 3 * kTabCopies * kBWinCopy * 4);
         tma_load_3d(sm.q[s], &tq, &sm.qd_full[s], 0, i0, bh);
         tma_load_3d(sm.dO[s], &tdo, &sm.qd_full[s], 0, i0, bh);
+        if (t == 0) grid_dep_wait();  // the windows come from the preprocess
         // Window: table indices tab_off + i0 - j0 - 128 + [0, kBWin), which
         // start at tab_len - kBWin minus that base in the reversed rows.
         const float* src = a.table + static_cast<size_t>(h) * a.tab_len +
@@ -687,9 +691,13 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
     }
     __syncthreads();
   }
-  // Last CTA: per-head outputs.
-  __threadfence();
-  if (threadIdx.x == 0) last = (atomicAdd(a.counter, 1) == static_cast<int>(gridDim.x) - 1);
+  // Last CTA: per-head outputs.  The barrier orders this CTA's atomics
+  // before thread 0's fence and count (one fence per CTA, not per thread).
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = (atomicAdd(a.counter, 1) == static_cast<int>(gridDim.x) - 1);
+  }
   __syncthreads();
   if (!last) return;
   __threadfence();

@@ -136,10 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    // The distance table (and the cleared status word) come from the
-    // previous kernel of this call.
-    grid_dep_wait();
-    sm.abort_flag = *reinterpret_cast<volatile int*>(&a.status->abort);
+    sm.abort_flag = 0;
     mbar_init(&sm.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
@@ -163,6 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = sm.tmem_base;
+  // The distance table and the cleared status word come from the previous
+  // kernel of this call.  Only the producer runs ahead of it (its Q, K and V
+  // loads need nothing from it); every other thread waits here, before its
+  // first look at the status word.
+  if (warp != 8) grid_dep_wait();
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes + kTabCopies * kWinCopy * 4);
         tma_load_3d(sm.k[s], &tk, &sm.k_full[s], 0, 128 * j, bh);
+        if (j == 0) grid_dep_wait();  // the windows come from the table kernel
         for (int k = 0; k < kTabCopies; ++k)
           bulk_load(sm.win[s] + win_copy_off(k, kWinCopyStride), tab_h + k * copy_stride + 128 * j,
                     kWinCopy * 4, &sm.k_full[s]);
