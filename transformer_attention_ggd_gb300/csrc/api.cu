@@ -352,10 +352,12 @@ bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void*
   cudaError_t e =
       launch_kernel(BAM_KERNEL_BWD_PREP, stream, [&] { return launch_bwd_prep(ba, stream); });
   if (e != cudaSuccess) return BAM_ERR_CUDA;
-  CUtensorMap tdq;
-  if (!encode_acc_rows(&tdq, ba.dq_acc, BH, T)) return BAM_ERR_CUDA;
+  CUtensorMap tdq, tdk, tdv;
+  if (!encode_acc_rows(&tdq, ba.dq_acc, BH, T) || !encode_rows(&tdk, dk, BH, T) ||
+      !encode_rows(&tdv, dv, BH, T))
+    return BAM_ERR_CUDA;
   e = launch_kernel(BAM_KERNEL_BWD, stream,
-                    [&] { return launch_bwd(tq, tk, tv, tdo, tdq, ba, stream); });
+                    [&] { return launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, ba, stream); });
   if (e != cudaSuccess) return BAM_ERR_CUDA;
   e = launch_kernel(BAM_KERNEL_BWD_FINAL, stream, [&] { return launch_bwd_final(ba, stream); });
   return cuda_status(e);

@@ -175,8 +175,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
-                       cudaStream_t st);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st);
 
 // Decode split geometry.

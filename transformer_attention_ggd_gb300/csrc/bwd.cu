@@ -16,8 +16,10 @@
 // C_i = sum_j P_ij dP_ij, and the final kernel adds sum_i (Delta_i - C_i) B_i:
 //   sum_ij P_ij (dP_ij - C_i) X_ij = sum_ij dS_ij X_ij + sum_i (Delta_i - C_i) B_i.
 //
-// One CTA owns a 128-key tile of one (b, h) and walks the 128-row query
-// tiles that see it:
+// Persistent: one CTA per SM walks a list of work items, each a 128-key
+// tile of one (b, h), and for each the 128-row query tiles that see it (the
+// next item's K/V and first S/dP overlap the current item's last tile and
+// its dK/dV epilogue):
 //   warp 16    TMA producer: K, V once; per query tile Q, dO and the three
 //              256-entry distance windows (b, db/dbeta, db/dmu, four shifted
 //              reversed copies each for 16-byte loads), 2 stages.
@@ -71,10 +73,14 @@ struct __align__(1024) BwdSmem {
   uint8_t dst[2 * kTile];  // (c dS)^T, same layout
   float dqs[2][128][32];   // dQ tile staged for the TMA reduction: two 128-B-swizzled boxes
   float win[kBStages][3][kBWinPlane];  // b, db/dbeta, db/dmu: four reversed copies each
-  float red[kBCompute][4];
+  float red[2][kBCompute][4];  // per-item scalar sums, by item parity
   uint64_t kv_full;
+  uint64_t k_empty;   // the item's K no longer read (after its last dQ product)
+  uint64_t v_empty;   // the item's V no longer read (after its last dP product)
   uint64_t dqs_full;
   uint64_t dqs_free;
+  uint64_t epi_full;   // dK/dV of an item staged (bf16) in the P^T buffer
+  uint64_t epi_free;   // that staging read by its TMA stores
   uint64_t qd_full[kBStages];
   uint64_t qd_empty[kBStages];
   uint64_t s_full;
@@ -108,6 +114,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, DevSta
   return __all_sync(0xffffffffu, ok);
 }
 
+// Barrier 1 over the element-wise warps, returning whether every thread
+// passed ok != 0 (all of them reach it once per work item).
+__device__ __forceinline__ int elementwise_barrier_and(int ok) {
+  int all;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 q, %1, 0;\n bar.red.and.pred p, 1, %2, q;\n"
+      " selp.s32 %0, 1, 0, p;\n}\n"
+      : "=r"(all)
+      : "r"(ok), "n"(32 * kBCompute)
+      : "memory");
+  return all;
+}
+
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
                "f"(c), "f"(d)
@@ -123,29 +142,45 @@ __device__ __forceinline__ uint32_t mn_chunk_offset(int m8, int k) {
   return (m8 >> 3) * kTile + (k >> 3) * 1024 + (k & 7) * 128 + (((m8 & 7) ^ (k & 7)) << 4);
 }
 
+// Work item w of a persistent CTA: key tile kb of head bh.  Items are in
+// longest-first order (causal: kb = 0 sees every query tile) and dealt out in
+// rounds, alternating direction ("snake") so that long and short items mix.
+struct BwdItem {
+  int kb, bh, h, j0, q_first, nq;
+};
+
+__device__ __forceinline__ bool bwd_item(const BwdArgs& a, int round, BwdItem& it) {
+  const int BH = a.B * a.H;
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int idx = round * G + ((round & 1) ? (G - 1 - c) : c);
+  if (idx >= a.nkb * BH) return false;
+  it.kb = idx / BH;
+  it.bh = idx % BH;
+  it.h = it.bh % a.H;
+  it.j0 = it.kb * 128;
+  it.q_first = a.causal ? it.kb : 0;
+  it.nq = a.nkb - it.q_first;
+  return true;
+}
+
 __global__ void __launch_bounds__(kBThreads, 1)
     bam_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                   const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
+                   const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
+                   const __grid_constant__ CUtensorMap tdv, const BwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // Aligned by an offset from the shared array itself (not through an
   // integer cast), so that accesses stay in the shared address space.
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw + ((0u - smem_u32(smem_raw)) & 1023u));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int BH = a.B * a.H;
-  const int kb = static_cast<int>(blockIdx.x) / BH;  // causal: most query tiles first
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int h = bh % a.H;
-  const int j0 = kb * 128;
-  const int nqt = (a.T + 127) / 128;
-  const int q_first = a.causal ? kb : 0;
-  const int nq = nqt - q_first;
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
     mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.k_empty, 1);
+    mbar_init(&sm.v_empty, 1);
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(&sm.qd_full[s], 1);
       mbar_init(&sm.qd_empty[s], 1);
@@ -155,6 +190,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
     mbar_init(&sm.ds_ready, kBCompute);
     mbar_init(&sm.dqs_full, kBCompute);
     mbar_init(&sm.dqs_free, 1);
+    mbar_init(&sm.epi_full, kBCompute);
+    mbar_init(&sm.epi_free, 1);
     mbar_init(&sm.mma_done, 1);
     mbar_init(&sm.mma_final, 1);
     fence_barrier_init();
@@ -175,46 +212,61 @@ __global__ void __launch_bounds__(kBThreads, 1)
   const size_t copy_stride = static_cast<size_t>(a.H) * a.tab_len;  // floats between copies
   const size_t plane = kTabCopies * copy_stride;
 
+  // Barrier phases: per query tile g (counted over all items of this CTA)
+  // for the Q/dO ring and the tile hand-offs; per item n for K/V.
   if (warp == kBProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = (*ab == 0);
-      bool kv_issued = false;
-      int issued = 0;
-      if (ok) {
-        prefetch_tmap(&tq);
-        prefetch_tmap(&tk);
-        prefetch_tmap(&tv);
-        prefetch_tmap(&tdo);
-        mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
-        tma_load_3d(sm.k, &tk, &sm.kv_full, 0, j0, bh);
-        tma_load_3d(sm.v, &tv, &sm.kv_full, 0, j0, bh);
-        kv_issued = true;
-      }
-      for (int t = 0; ok && t < nq; ++t) {
-        const int s = t % kBStages;
-        const int i0 = (q_first + t) * 128;
-        if (t >= kBStages) {
-          ok = mbar_wait(&sm.qd_empty[s], ((t / kBStages) - 1) & 1, a.status, ab, kSiteBProd);
-          if (!ok) break;
+      int g = 0, n = 0;
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      BwdItem it;
+      for (int round = 0; ok && bwd_item(a, round, it); ++round) {
+        for (int t = 0; ok && t < it.nq; ++t, ++g) {
+          const int s = g % kBStages;
+          const int i0 = (it.q_first + t) * 128;
+          if (g >= kBStages) {
+            ok = mbar_wait(&sm.qd_empty[s], ((g / kBStages) - 1) & 1, a.status, ab, kSiteBProd);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTile + 3 * kTabCopies * kBWinCopy * 4);
+          tma_load_3d(sm.q[s], &tq, &sm.qd_full[s], 0, i0, it.bh);
+          tma_load_3d(sm.dO[s], &tdo, &sm.qd_full[s], 0, i0, it.bh);
+          if (g == 0) grid_dep_wait();  // the windows come from the preprocess
+          // Window: table indices tab_off + i0 - j0 - 128 + [0, kBWin), which
+          // start at tab_len - kBWin minus that base in the reversed rows.
+          const float* src = a.table + static_cast<size_t>(it.h) * a.tab_len +
+                             (a.tab_len - kBWin - (a.tab_off + i0 - it.j0 - 128));
+          for (int p = 0; p < 3; ++p)
+            for (int k = 0; k < kTabCopies; ++k)
+              bulk_load(sm.win[s][p] + win_copy_off(k, kBWinCopyStride),
+                        src + p * plane + k * copy_stride, kBWinCopy * 4, &sm.qd_full[s]);
+          if (t == 0) {
+            // K and V of the item into the single K/V buffers: V as soon as
+            // the previous item's last dP product is done, K after its last
+            // dQ product (issued first among that tile's gradient products).
+            mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
+            if (n > 0) {
+              ok = mbar_wait(&sm.v_empty, (n - 1) & 1, a.status, ab, kSiteBProd);
+              if (!ok) break;
+            }
+            tma_load_3d(sm.v, &tv, &sm.kv_full, 0, it.j0, it.bh);
+            if (n > 0) {
+              ok = mbar_wait(&sm.k_empty, (n - 1) & 1, a.status, ab, kSiteBProd);
+              if (!ok) break;
+            }
+            tma_load_3d(sm.k, &tk, &sm.kv_full, 0, it.j0, it.bh);
+            ++n;
+          }
         }
-        mbar_arrive_expect_tx(&sm.qd_full[s], 2 * kTile + 3 * kTabCopies * kBWinCopy * 4);
-        tma_load_3d(sm.q[s], &tq, &sm.qd_full[s], 0, i0, bh);
-        tma_load_3d(sm.dO[s], &tdo, &sm.qd_full[s], 0, i0, bh);
-        if (t == 0) grid_dep_wait();  // the windows come from the preprocess
-        // Window: table indices tab_off + i0 - j0 - 128 + [0, kBWin), which
-        // start at tab_len - kBWin minus that base in the reversed rows.
-        const float* src = a.table + static_cast<size_t>(h) * a.tab_len +
-                           (a.tab_len - kBWin - (a.tab_off + i0 - j0 - 128));
-        for (int p = 0; p < 3; ++p)
-          for (int k = 0; k < kTabCopies; ++k)
-            bulk_load(sm.win[s][p] + win_copy_off(k, kBWinCopyStride),
-                      src + p * plane + k * copy_stride, kBWinCopy * 4, &sm.qd_full[s]);
-        issued = t + 1;
       }
-      if (kv_issued) mbar_drain(&sm.kv_full, 0);
-      for (int t = max(0, issued - kBStages); t < issued; ++t)
-        mbar_drain(&sm.qd_full[t % kBStages], (t / kBStages) & 1);
+      // Copies still in flight land before this CTA leaves.
+      if (n > 0) mbar_drain(&sm.kv_full, (n - 1) & 1);
+      for (int x = max(0, g - kBStages); x < g; ++x)
+        mbar_drain(&sm.qd_full[x % kBStages], (x / kBStages) & 1);
     }
   } else if (warp == kBMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -236,7 +288,12 @@ __global__ void __launch_bounds__(kBThreads, 1)
       const uint64_t kM = sdesc_sw128(smem_u32(sm.k), kTile, 1024);
       const uint64_t ptM = sdesc_sw128(smem_u32(sm.pt), kTile, 1024);
       const uint64_t dsM = sdesc_sw128(smem_u32(sm.dst), kTile, 1024);
-      auto issue_s_dp = [&](int s) {
+      // S and dP of global tile g (stage g % 2) once its Q/dO are in; the
+      // caller has made sure the S/dP columns are free and K/V are in.
+      auto issue_s_dp = [&](int g) -> bool {
+        const int s = g % kBStages;
+        if (!mbar_wait(&sm.qd_full[s], (g / kBStages) & 1, a.status, ab, kSiteBMmaQD)) return false;
+        tc_fence_after();
         const uint64_t qd = qK0 + kTileDesc * s, dd = dK0 + kTileDesc * s;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -245,40 +302,62 @@ __global__ void __launch_bounds__(kBThreads, 1)
         for (int kk = 0; kk < 4; ++kk)
           umma_ss(tm + kColDP, dd + 2 * kk, vK + 2 * kk, idSP, kk > 0 ? 1u : 0u);
         umma_commit(&sm.s_full);
+        return true;
       };
-      if (ok) ok = mbar_wait(&sm.kv_full, 0, a.status, ab, kSiteBMmaKV);
-      if (ok && nq > 0) ok = mbar_wait(&sm.qd_full[0], 0, a.status, ab, kSiteBMmaQD);
-      if (ok && nq > 0) {
-        tc_fence_after();
-        issue_s_dp(0);
+      int g = 0, n = 0;
+      BwdItem it, nxt;
+      bool have = bwd_item(a, 0, it);
+      if (ok && have) {
+        ok = mbar_wait(&sm.kv_full, 0, a.status, ab, kSiteBMmaKV);
+        if (ok) ok = issue_s_dp(0);
+        if (ok && it.nq == 1) umma_commit(&sm.v_empty);  // that was the item's last dP
       }
-      for (int t = 0; ok && t < nq; ++t) {
-        const int s = t % kBStages;
-        // S and dP of the next tile once this tile's S/dP columns are read.
-        if (t + 1 < nq) {
-          ok = mbar_wait(&sm.sdp_free, t & 1, a.status, ab, kSiteBMmaFree);
-          if (!ok) break;
-          ok = mbar_wait(&sm.qd_full[(t + 1) % kBStages], ((t + 1) / kBStages) & 1, a.status, ab,
-                         kSiteBMmaQD);
+      for (int round = 0; ok && have; ++round) {
+        const bool have_next = bwd_item(a, round + 1, nxt);
+        for (int t = 0; ok && t < it.nq; ++t, ++g) {
+          const int s = g % kBStages;
+          // S and dP of the item's next tile once this tile's S/dP columns
+          // are read (they overlap this tile's last element-wise chunk).
+          if (t + 1 < it.nq) {
+            ok = mbar_wait(&sm.sdp_free, g & 1, a.status, ab, kSiteBMmaFree);
+            if (!ok) break;
+            ok = issue_s_dp(g + 1);
+            if (!ok) break;
+            if (t + 2 == it.nq) umma_commit(&sm.v_empty);  // the item's last dP
+          }
+          ok = mbar_wait(&sm.ds_ready, g & 1, a.status, ab, kSiteBMmaDS);
           if (!ok) break;
           tc_fence_after();
-          issue_s_dp((t + 1) % kBStages);
+          const uint64_t qd = qM0 + kTileDesc * s, dd = dM0 + kTileDesc * s;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ = (c dS) K
+            umma_ts(tm + kColDQ, tm + kColDS + 8 * kk, kM + 128 * kk, idQ, kk > 0 ? 1u : 0u);
+          if (t + 1 == it.nq) umma_commit(&sm.k_empty);  // the item's last use of K
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
+            umma_ss(tm + kColDV, ptM + 128 * kk, dd + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dK += (c dS)^T Q
+            umma_ss(tm + kColDK, dsM + 128 * kk, qd + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&sm.mma_done);
+          umma_commit(&sm.qd_empty[s]);
+          if (t + 1 == it.nq) {
+            ++n;
+            if (have_next) {
+              // First S/dP of the next item: its K/V in and this tile's
+              // S/dP columns read.
+              ok = mbar_wait(&sm.kv_full, n & 1, a.status, ab, kSiteBMmaKV);
+              if (!ok) break;
+              ok = mbar_wait(&sm.sdp_free, g & 1, a.status, ab, kSiteBMmaFree);
+              if (!ok) break;
+              ok = issue_s_dp(g + 1);
+              if (!ok) break;
+              if (nxt.nq == 1) umma_commit(&sm.v_empty);  // the next item's last dP
+            }
+          }
         }
-        ok = mbar_wait(&sm.ds_ready, t & 1, a.status, ab, kSiteBMmaDS);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t qd = qM0 + kTileDesc * s, dd = dM0 + kTileDesc * s;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
-          umma_ss(tm + kColDV, ptM + 128 * kk, dd + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dK += (c dS)^T Q
-          umma_ss(tm + kColDK, dsM + 128 * kk, qd + 128 * kk, idKV, (t > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ = (c dS) K
-          umma_ts(tm + kColDQ, tm + kColDS + 8 * kk, kM + 128 * kk, idQ, kk > 0 ? 1u : 0u);
-        umma_commit(&sm.mma_done);
-        umma_commit(&sm.qd_empty[s]);
+        it = nxt;
+        have = have_next;
       }
       umma_commit(&sm.mma_final);
       mbar_drain(&sm.mma_final, 0);
@@ -287,15 +366,28 @@ __global__ void __launch_bounds__(kBThreads, 1)
     // ------------------------------------------------------------ dQ reducer
     if (lane == 0) {
       bool ok = (*ab == 0);
-      for (int t = 0; ok && t < nq; ++t) {
-        ok = mbar_wait(&sm.dqs_full, t & 1, a.status, ab, kSiteBDq);
+      int g = 0;
+      BwdItem it;
+      for (int round = 0; ok && bwd_item(a, round, it); ++round) {
+        for (int t = 0; ok && t < it.nq; ++t, ++g) {
+          ok = mbar_wait(&sm.dqs_full, g & 1, a.status, ab, kSiteBDq);
+          if (!ok) break;
+          const int i0 = (it.q_first + t) * 128;
+          tma_reduce_add_3d(&tdq, sm.dqs[0], 0, i0, it.bh);
+          tma_reduce_add_3d(&tdq, sm.dqs[1], 32, i0, it.bh);
+          bulk_commit();
+          bulk_wait_read_all();  // staging tile read: it may be written again
+          mbar_arrive(&sm.dqs_free);
+        }
         if (!ok) break;
-        const int i0 = (q_first + t) * 128;
-        tma_reduce_add_3d(&tdq, sm.dqs[0], 0, i0, bh);
-        tma_reduce_add_3d(&tdq, sm.dqs[1], 32, i0, bh);
+        // The item's dK and dV rows (bf16, staged in the P^T buffer).
+        ok = mbar_wait(&sm.epi_full, round & 1, a.status, ab, kSiteBDq);
+        if (!ok) break;
+        tma_store_3d(&tdk, sm.pt, 0, it.j0, it.bh);
+        tma_store_3d(&tdv, sm.pt + kTile, 0, it.j0, it.bh);
         bulk_commit();
-        bulk_wait_read_all();  // staging tile read: it may be written again
-        mbar_arrive(&sm.dqs_free);
+        bulk_wait_read_all();
+        mbar_arrive(&sm.epi_free);
       }
       // The staging tile must stay valid until the last reduction has read
       // it; the writes themselves complete with the grid.
@@ -308,12 +400,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
     const uint32_t lb = tmem_lane_base(warp);
     const int kq = (r + 1) & 3;
     const int wrev = win_copy_off(kq, kBWinCopyStride) + (127 - r + kq);
-    const float s_h = a.ssmax ? __ldg(a.s + h) : 1.0f;
-    // Scalar-gradient sums as f32x2 pairs (even / odd key columns):
-    // sum dS b (log2 units), sum dS db/dbeta, sum dS db/dmu, and sum over
-    // rows of w_i * sum_j dS S.
-    uint64_t accB2 = 0ull, accBeta2 = 0ull, accMu2 = 0ull;
-    float acc_s = 0.f;
     bool ok = (*ab == 0);
     // dQ of a finished query tile: TMEM -> shared staging tile (two
     // 128-byte-swizzled 32-column boxes) for the dQ warp's TMA reductions.
@@ -341,219 +427,243 @@ __global__ void __launch_bounds__(kBThreads, 1)
       ++n_dq;
       return true;
     };
-    // LSE and Delta of this thread's row, one query tile ahead.
-    float lse_nx = 0.f, del_nx = 0.f;
-    {
-      const int i = q_first * 128 + r;
-      if (nq > 0 && i < a.T) {
-        lse_nx = __ldg(a.lse + static_cast<size_t>(bh) * a.T + i);
-        del_nx = __ldg(a.delta + static_cast<size_t>(bh) * a.T + i);
-      }
-    }
-    for (int t = 0; ok && t < nq; ++t) {
-      const int s = t % kBStages;
-      const int i0 = (q_first + t) * 128;
-      const int i = i0 + r;
-      const bool row_ok = i < a.T;
-      const float lse_row = lse_nx, del_row = del_nx;
-      if (t + 1 < nq && i + 128 < a.T) {
-        lse_nx = __ldg(a.lse + static_cast<size_t>(bh) * a.T + i + 128);
-        del_nx = __ldg(a.delta + static_cast<size_t>(bh) * a.T + i + 128);
-      }
-      // Per-row constants.
-      const float n = a.causal ? static_cast<float>(i + 1) : static_cast<float>(a.T);
-      const float w_ln = logf(n) * 0.125f;             // ln(n_i)/sqrt(D)
-      const float cn = a.ssmax ? s_h * w_ln : 0.125f;   // c_i
-      const float cr = cn * 1.44269504088896341f;      // c_i log2(e)
-      const size_t ridx = static_cast<size_t>(bh) * a.T + i;
-      const float lse2 = row_ok ? lse_row * 1.44269504088896341f : INFINITY;
-      const float delta = row_ok ? del_row : 0.0f;
-      int lim = a.T - 1 - j0;              // last visible key column
-      if (a.causal) lim = min(lim, i - j0);
-      const uint64_t cr2 = f2_pack(cr, cr), cn2 = f2_pack(cn, cn);
-      const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndel2 = f2_pack(-delta, -delta);
-
-      ok = warp_wait(&sm.s_full, t & 1, a.status, ab, kSiteBWgS);
-      if (!ok) break;
-      ok = warp_wait(&sm.qd_full[s], (t / kBStages) & 1, a.status, ab, kSiteBWgQD);
-      if (!ok) break;
-      tc_fence_after();
-      // Key c of row r reads window entry 128 + r - c, i.e. reversed entry
-      // 127 - r + c; in copy kq the entries of c, c+1, c+2, c+3 (c % 4 == 0)
-      // form one aligned 16-byte vector.
-      const float* wv = sm.win[s][0] + wrev;
-      // Row partial sums for the Delta correction and the SSMax sum.
-      uint64_t pB2 = 0ull, pBeta2 = 0ull, pMu2 = 0ull, pS2 = 0ull, pDP2 = 0ull, rowSS2 = 0ull;
-      // P and c*dS of keys [c0, c0+8) of query row r into the MN-major
-      // operands (one 16-byte chunk each) and c*dS into TMEM.
-      auto store_chunk = [&](int c0, const uint32_t* pp, const uint32_t* dd) {
-        const uint32_t off = mn_chunk_offset(c0 / 8, r);
-        *reinterpret_cast<uint4*>(sm.pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
-        *reinterpret_cast<uint4*>(sm.dst + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
-        tmem_st_32x32b_x4(tm + lb + kColDS + c0 / 2, dd);
-      };
-      uint32_t pp_prev[4], dd_prev[4];  // chunk computed, not yet stored
-      // Four 8-key chunks of S and dP per thread.
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        const int c0 = kBKeysPerWarp * hc + 8 * ch;
-        uint32_t sv[8], dpv[8];
-        tmem_ld_32x32b_x8(tm + lb + kColS + c0, sv);
-        tmem_ld_32x32b_x8(tm + lb + kColDP + c0, dpv);
-        uint64_t tb[4], tbeta[4], tmu[4];
-        const float* wp = wv + c0;
-        ld_f2x2(wp, tb[0], tb[1]);
-        ld_f2x2(wp + 4, tb[2], tb[3]);
-        ld_f2x2(wp + kBWinPlane, tbeta[0], tbeta[1]);
-        ld_f2x2(wp + kBWinPlane + 4, tbeta[2], tbeta[3]);
-        ld_f2x2(wp + 2 * kBWinPlane, tmu[0], tmu[1]);
-        ld_f2x2(wp + 2 * kBWinPlane + 4, tmu[2], tmu[3]);
-        tmem_ld_wait();
-        reg_fence8(sv);
-        reg_fence8(dpv);
-        if (ch == 3) {
-          // This warp's last S/dP columns of the tile are in registers: the
-          // next tile's S and dP may be written over them.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.sdp_free);
+    int g = 0;
+    BwdItem it;
+    for (int round = 0; ok && bwd_item(a, round, it); ++round) {
+      const int bh = it.bh, j0 = it.j0, q_first = it.q_first, nq = it.nq;
+      const float s_h = a.ssmax ? __ldg(a.s + it.h) : 1.0f;
+      // Scalar-gradient sums of the item as f32x2 pairs (even / odd key
+      // columns): sum dS b (log2 units), sum dS db/dbeta, sum dS db/dmu, and
+      // sum over rows of w_i * sum_j dS S.
+      uint64_t accB2 = 0ull, accBeta2 = 0ull, accMu2 = 0ull;
+      float acc_s = 0.f;
+      // LSE and Delta of this thread's row, one query tile ahead.
+      float lse_nx = 0.f, del_nx = 0.f;
+      {
+        const int i = q_first * 128 + r;
+        if (i < a.T) {
+          lse_nx = __ldg(a.lse + static_cast<size_t>(bh) * a.T + i);
+          del_nx = __ldg(a.delta + static_cast<size_t>(bh) * a.T + i);
         }
-        uint32_t pp[4], dd[4];
-        // Masked keys (past the causal limit or T) only in chunks that reach
-        // them; the test is warp-uniform so each warp takes one version.
-        auto elementwise = [&](auto masked) {
+      }
+      for (int t = 0; ok && t < nq; ++t, ++g) {
+        const int s = g % kBStages;
+        const int i0 = (q_first + t) * 128;
+        const int i = i0 + r;
+        const bool row_ok = i < a.T;
+        const float lse_row = lse_nx, del_row = del_nx;
+        if (t + 1 < nq && i + 128 < a.T) {
+          lse_nx = __ldg(a.lse + static_cast<size_t>(bh) * a.T + i + 128);
+          del_nx = __ldg(a.delta + static_cast<size_t>(bh) * a.T + i + 128);
+        }
+        // Per-row constants.
+        const float n = a.causal ? static_cast<float>(i + 1) : static_cast<float>(a.T);
+        const float w_ln = logf(n) * 0.125f;             // ln(n_i)/sqrt(D)
+        const float cn = a.ssmax ? s_h * w_ln : 0.125f;   // c_i
+        const float cr = cn * 1.44269504088896341f;      // c_i log2(e)
+        const size_t ridx = static_cast<size_t>(bh) * a.T + i;
+        const float lse2 = row_ok ? lse_row * 1.44269504088896341f : INFINITY;
+        const float delta = row_ok ? del_row : 0.0f;
+        int lim = a.T - 1 - j0;              // last visible key column
+        if (a.causal) lim = min(lim, i - j0);
+        const uint64_t cr2 = f2_pack(cr, cr), cn2 = f2_pack(cn, cn);
+        const uint64_t nlse2 = f2_pack(-lse2, -lse2), ndel2 = f2_pack(-delta, -delta);
+
+        ok = warp_wait(&sm.s_full, g & 1, a.status, ab, kSiteBWgS);
+        if (!ok) break;
+        ok = warp_wait(&sm.qd_full[s], (g / kBStages) & 1, a.status, ab, kSiteBWgQD);
+        if (!ok) break;
+        tc_fence_after();
+        // Key c of row r reads window entry 128 + r - c, i.e. reversed entry
+        // 127 - r + c; in copy kq the entries of c, c+1, c+2, c+3 (c % 4 == 0)
+        // form one aligned 16-byte vector.
+        const float* wv = sm.win[s][0] + wrev;
+        // Row partial sums for the Delta correction and the SSMax sum.
+        uint64_t pB2 = 0ull, pBeta2 = 0ull, pMu2 = 0ull, pS2 = 0ull, pDP2 = 0ull, rowSS2 = 0ull;
+        // P and c*dS of keys [c0, c0+8) of query row r into the MN-major
+        // operands (one 16-byte chunk each) and c*dS into TMEM.
+        auto store_chunk = [&](int c0, const uint32_t* pp, const uint32_t* dd) {
+          const uint32_t off = mn_chunk_offset(c0 / 8, r);
+          *reinterpret_cast<uint4*>(sm.pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
+          *reinterpret_cast<uint4*>(sm.dst + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
+          tmem_st_32x32b_x4(tm + lb + kColDS + c0 / 2, dd);
+        };
+        uint32_t pp_prev[4], dd_prev[4];  // chunk computed, not yet stored
+        // Four 8-key chunks of S and dP per thread.
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          const int c0 = kBKeysPerWarp * hc + 8 * ch;
+          uint32_t sv[8], dpv[8];
+          tmem_ld_32x32b_x8(tm + lb + kColS + c0, sv);
+          tmem_ld_32x32b_x8(tm + lb + kColDP + c0, dpv);
+          uint64_t tb[4], tbeta[4], tmu[4];
+          const float* wp = wv + c0;
+          ld_f2x2(wp, tb[0], tb[1]);
+          ld_f2x2(wp + 4, tb[2], tb[3]);
+          ld_f2x2(wp + kBWinPlane, tbeta[0], tbeta[1]);
+          ld_f2x2(wp + kBWinPlane + 4, tbeta[2], tbeta[3]);
+          ld_f2x2(wp + 2 * kBWinPlane, tmu[0], tmu[1]);
+          ld_f2x2(wp + 2 * kBWinPlane + 4, tmu[2], tmu[3]);
+          tmem_ld_wait();
+          reg_fence8(sv);
+          reg_fence8(dpv);
+          if (ch == 3) {
+            // This warp's last S/dP columns of the tile are in registers: the
+            // next tile's S and dP may be written over them.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.sdp_free);
+          }
+          uint32_t pp[4], dd[4];
+          // Masked keys (past the causal limit or T) only in chunks that reach
+          // them; the test is warp-uniform so each warp takes one version.
+          auto elementwise = [&](auto masked) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const int c = c0 + 2 * x;
+              const uint64_t s2 =
+                  f2_pack(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
+              const uint64_t dp2 =
+                  f2_pack(__uint_as_float(dpv[2 * x]), __uint_as_float(dpv[2 * x + 1]));
+              float z0, z1;
+              f2_unpack(fadd2(ffma2(s2, cr2, tb[x]), nlse2), z0, z1);
+              if constexpr (decltype(masked)::value) {
+                if (c > lim) z0 = -INFINITY;
+                if (c + 1 > lim) z1 = -INFINITY;
+              }
+              const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+              const uint64_t p2 = f2_pack(p0, p1);
+              const uint64_t dS2 = fmul2(p2, fadd2(dp2, ndel2));
+              accB2 = ffma2(dS2, tb[x], accB2);
+              accBeta2 = ffma2(dS2, tbeta[x], accBeta2);
+              accMu2 = ffma2(dS2, tmu[x], accMu2);
+              rowSS2 = ffma2(dS2, s2, rowSS2);
+              pB2 = ffma2(p2, tb[x], pB2);
+              pBeta2 = ffma2(p2, tbeta[x], pBeta2);
+              pMu2 = ffma2(p2, tmu[x], pMu2);
+              pS2 = ffma2(p2, s2, pS2);
+              pDP2 = ffma2(p2, dp2, pDP2);
+              pp[x] = pack_bf16x2(p0, p1);
+              float q0, q1;
+              f2_unpack(fmul2(dS2, cn2), q0, q1);
+              dd[x] = pack_bf16x2(q0, q1);
+            }
+          };
+          if (__any_sync(0xffffffffu, c0 + 7 > lim))
+            elementwise(std::true_type{});
+          else
+            elementwise(std::false_type{});
+          if (ch == 1 && t > 0) {
+            // The previous tile's gradient products must be done before its
+            // P^T / dS^T buffers and dS TMEM are overwritten; its dQ tile is
+            // drained here, before this tile's dQ product is issued.  (The
+            // previous item's last tile was drained at that item's end.)
+            ok = warp_wait(&sm.mma_done, (g - 1) & 1, a.status, ab, kSiteBWgDone);
+            if (!ok) break;
+            tc_fence_after();
+            if (!dq_epilogue()) {
+              ok = false;
+              break;
+            }
+          }
+          if (ch == 1 && t == 0 && round > 0) {
+            // The previous item's dK/dV staging in the P^T buffer is read.
+            ok = warp_wait(&sm.epi_free, (round - 1) & 1, a.status, ab, kSiteBWgDq);
+            if (!ok) break;
+          }
+          if (ch > 0) store_chunk(c0 - 8, pp_prev, dd_prev);
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            const int c = c0 + 2 * x;
-            const uint64_t s2 =
-                f2_pack(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
-            const uint64_t dp2 =
-                f2_pack(__uint_as_float(dpv[2 * x]), __uint_as_float(dpv[2 * x + 1]));
-            float z0, z1;
-            f2_unpack(fadd2(ffma2(s2, cr2, tb[x]), nlse2), z0, z1);
-            if constexpr (decltype(masked)::value) {
-              if (c > lim) z0 = -INFINITY;
-              if (c + 1 > lim) z1 = -INFINITY;
-            }
-            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-            const uint64_t p2 = f2_pack(p0, p1);
-            const uint64_t dS2 = fmul2(p2, fadd2(dp2, ndel2));
-            accB2 = ffma2(dS2, tb[x], accB2);
-            accBeta2 = ffma2(dS2, tbeta[x], accBeta2);
-            accMu2 = ffma2(dS2, tmu[x], accMu2);
-            rowSS2 = ffma2(dS2, s2, rowSS2);
-            pB2 = ffma2(p2, tb[x], pB2);
-            pBeta2 = ffma2(p2, tbeta[x], pBeta2);
-            pMu2 = ffma2(p2, tmu[x], pMu2);
-            pS2 = ffma2(p2, s2, pS2);
-            pDP2 = ffma2(p2, dp2, pDP2);
-            pp[x] = pack_bf16x2(p0, p1);
-            float q0, q1;
-            f2_unpack(fmul2(dS2, cn2), q0, q1);
-            dd[x] = pack_bf16x2(q0, q1);
-          }
-        };
-        if (__any_sync(0xffffffffu, c0 + 7 > lim))
-          elementwise(std::true_type{});
-        else
-          elementwise(std::false_type{});
-        if (ch == 1 && t > 0) {
-          // The previous tile's gradient products must be done before its
-          // P^T / dS^T buffers and dS TMEM are overwritten; its dQ tile is
-          // drained here, before this tile's dQ product is issued.
-          ok = warp_wait(&sm.mma_done, (t - 1) & 1, a.status, ab, kSiteBWgDone);
-          if (!ok) break;
-          tc_fence_after();
-          if (!dq_epilogue()) {
-            ok = false;
-            break;
+            pp_prev[x] = pp[x];
+            dd_prev[x] = dd[x];
           }
         }
-        if (ch > 0) store_chunk(c0 - 8, pp_prev, dd_prev);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          pp_prev[x] = pp[x];
-          dd_prev[x] = dd[x];
+        if (!ok) break;
+        store_chunk(kBKeysPerWarp * hc + 24, pp_prev, dd_prev);
+        {
+          float a0, a1;
+          f2_unpack(rowSS2, a0, a1);
+          acc_s = fmaf(a0 + a1, w_ln, acc_s);
         }
+        if (row_ok) {
+          float b0, b1, e0, e1, m0, m1, s0, s1, d0, d1;
+          f2_unpack(pB2, b0, b1);
+          f2_unpack(pBeta2, e0, e1);
+          f2_unpack(pMu2, m0, m1);
+          f2_unpack(pS2, s0, s1);
+          f2_unpack(pDP2, d0, d1);
+          float* ra = a.rowacc + ridx * 8;
+          red_add_v4(ra, b0 + b1, e0 + e1, m0 + m1, (s0 + s1) * w_ln);
+          atomicAdd(ra + 4, d0 + d1);
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.ds_ready);
       }
-      if (!ok) break;
-      store_chunk(kBKeysPerWarp * hc + 24, pp_prev, dd_prev);
-      if (!ok) break;
+      // Block reduction of the item's scalar-gradient sums, one atomic per
+      // sum (while the item's last gradient products run).  Every
+      // element-wise warp gets here once per item, also after giving up.
+      float v4[4];
       {
         float a0, a1;
-        f2_unpack(rowSS2, a0, a1);
-        acc_s = fmaf(a0 + a1, w_ln, acc_s);
+        f2_unpack(accB2, a0, a1);
+        v4[0] = a0 + a1;
+        f2_unpack(accBeta2, a0, a1);
+        v4[1] = a0 + a1;
+        f2_unpack(accMu2, a0, a1);
+        v4[2] = a0 + a1;
+        v4[3] = acc_s;
       }
-      if (row_ok) {
-        float b0, b1, e0, e1, m0, m1, s0, s1, d0, d1;
-        f2_unpack(pB2, b0, b1);
-        f2_unpack(pBeta2, e0, e1);
-        f2_unpack(pMu2, m0, m1);
-        f2_unpack(pS2, s0, s1);
-        f2_unpack(pDP2, d0, d1);
-        float* ra = a.rowacc + ridx * 8;
-        red_add_v4(ra, b0 + b1, e0 + e1, m0 + m1, (s0 + s1) * w_ln);
-        atomicAdd(ra + 4, d0 + d1);
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v4[x] += __shfl_xor_sync(0xffffffffu, v4[x], off);
+      if (lane == 0)
+        for (int x = 0; x < 4; ++x) sm.red[round & 1][warp][x] = v4[x];
+      const int all_ok = elementwise_barrier_and(ok ? 1 : 0);
+      if (threadIdx.x < 4 && all_ok) {
+        float tot = 0.f;
+        for (int w = 0; w < kBCompute; ++w) tot += sm.red[round & 1][w][threadIdx.x];
+        atomicAdd(a.gacc + threadIdx.x * a.H + it.h, tot);
       }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.ds_ready);
-    }
-    // Block reduction of the scalar-gradient sums, one atomic per head and sum
-    // (while the last tile's gradient products run).
-    float v4[4];
-    {
-      float a0, a1;
-      f2_unpack(accB2, a0, a1);
-      v4[0] = a0 + a1;
-      f2_unpack(accBeta2, a0, a1);
-      v4[1] = a0 + a1;
-      f2_unpack(accMu2, a0, a1);
-      v4[2] = a0 + a1;
-      v4[3] = acc_s;
-    }
-#pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v4[x] += __shfl_xor_sync(0xffffffffu, v4[x], off);
-    if (lane == 0)
-      for (int x = 0; x < 4; ++x) sm.red[warp][x] = v4[x];
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kBCompute) : "memory");
-    if (threadIdx.x < 4 && ok) {
-      float tot = 0.f;
-      for (int w = 0; w < kBCompute; ++w) tot += sm.red[w][threadIdx.x];
-      atomicAdd(a.gacc + threadIdx.x * a.H + h, tot);
-    }
-    if (ok && nq > 0) {
-      ok = warp_wait(&sm.mma_done, (nq - 1) & 1, a.status, ab, kSiteBWgDone);
+      ok = all_ok;
       if (ok) {
-        tc_fence_after();
-        ok = dq_epilogue();
-      }
-      if (ok) {
-        // dK and dV rows: TMEM lane = key j0 + r; this warp writes 16 of the
-        // 64 dimensions.
-        const int j = j0 + r;
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t col = (which ? kColDV : kColDK) + 16 * hc;
-          uint32_t kvv[16];
-          tmem_ld_32x32b_x16(tm + lb + col, kvv);
-          tmem_ld_wait();
-          reg_fence16(kvv);
-          if (j < a.T) {
-            uint16_t* out =
-                (which ? a.dv : a.dk) + (static_cast<size_t>(bh) * a.T + j) * kHeadDim + 16 * hc;
-            uint4* o4 = reinterpret_cast<uint4*>(out);
+        // The item's last gradient products, then its dQ tile and the dK/dV
+        // rows (TMEM lane = key j0 + r; this warp writes 16 of the 64
+        // dimensions).  The next item's first dK/dV product comes after this
+        // warp's next ds_ready arrival, so these TMEM reads are done by then.
+        ok = warp_wait(&sm.mma_done, (g - 1) & 1, a.status, ab, kSiteBWgDone);
+        if (ok) {
+          tc_fence_after();
+          ok = dq_epilogue();
+        }
+        if (ok) {
+          // dK and dV rows as bf16 into the P^T buffer (free once the item's
+          // last products are done), 128-byte rows with the 128-byte swizzle,
+          // for the dQ warp's TMA stores: TMEM lane = key j0 + r; this warp
+          // holds 16 of the 64 dimensions (two 16-byte chunks of the row).
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t col = (which ? kColDV : kColDK) + 16 * hc;
+            uint32_t kvv[16];
+            tmem_ld_32x32b_x16(tm + lb + col, kvv);
+            tmem_ld_wait();
+            reg_fence16(kvv);
+            uint8_t* rowp = sm.pt + which * kTile + r * 128;
 #pragma unroll
-            for (int x = 0; x < 2; ++x)
-              o4[x] = make_uint4(
+            for (int x = 0; x < 2; ++x) {
+              const int cc = 2 * hc + x;
+              *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(
                   pack_bf16x2(__uint_as_float(kvv[8 * x]), __uint_as_float(kvv[8 * x + 1])),
                   pack_bf16x2(__uint_as_float(kvv[8 * x + 2]), __uint_as_float(kvv[8 * x + 3])),
                   pack_bf16x2(__uint_as_float(kvv[8 * x + 4]), __uint_as_float(kvv[8 * x + 5])),
                   pack_bf16x2(__uint_as_float(kvv[8 * x + 6]), __uint_as_float(kvv[8 * x + 7])));
+            }
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.epi_full);
         }
       }
     }
@@ -728,8 +838,8 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
-                       cudaStream_t st) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(BwdSmem) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -739,9 +849,18 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const unsigned grid = static_cast<unsigned>(a.nkb) * static_cast<unsigned>(a.B * a.H);
+  // Persistent: one CTA per SM (at most one per work item).
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  const long items = static_cast<long>(a.nkb) * a.B * a.H;
+  const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
   return launch_k(bam_bwd_kernel, dim3(grid), dim3(kBThreads), smem, st, true, tq, tk, tv, tdo,
-                  tdq, a);
+                  tdq, tdk, tdv, a);
 }
 
 cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
