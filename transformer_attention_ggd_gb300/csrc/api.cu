@@ -240,7 +240,11 @@ bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, in
   fa.o_fp32 = o_fp32 ? 1 : 0;
   fa.tab_len = g.len;
   fa.tab_off = g.off;
-  e = launch_kernel(BAM_KERNEL_FWD, stream, [&] { return launch_fwd(tq, tk, tv, fa, stream); });
+  // O by TMA stores: fp32 in 32-column boxes, bf16 in 64-column boxes.
+  CUtensorMap to;
+  if (!(o_fp32 ? encode_acc_rows(&to, o, BH, T) : encode_rows(&to, o, BH, T))) return BAM_ERR_CUDA;
+  e = launch_kernel(BAM_KERNEL_FWD, stream,
+                    [&] { return launch_fwd(tq, tk, tv, to, fa, stream); });
   return cuda_status(e);
 }
 

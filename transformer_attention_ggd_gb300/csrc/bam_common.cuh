@@ -170,7 +170,7 @@ inline int sm_count() {
 // Internal launchers (one per kernel).  Each returns the launch error.
 cudaError_t launch_table(const TableArgs& a, cudaStream_t st);
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, cudaStream_t st);
+                       const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st);

@@ -49,6 +49,9 @@ struct __align__(1024) FwdSmem {
   uint8_t q[2][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
+  // Normalised O of each query tile for its TMA store: fp32 as two
+  // 128-byte-swizzled boxes of 32 columns, or bf16 as one of 64 columns.
+  uint8_t ost[2][2 * kTileBytes];
   float win[kStages][kWinStage];
   uint64_t q_full;
   uint64_t k_full[kStages];
@@ -58,6 +61,7 @@ struct __align__(1024) FwdSmem {
   uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
+  uint64_t o_full[2];  // the tile's four softmax warps have staged their O rows
   uint64_t mma_final;
   uint32_t tmem_base;
   int abort_flag;
@@ -74,7 +78,8 @@ enum : int {
   kSiteSoftS = 30,
   kSiteSoftK = 31,
   kSiteSoftPV = 32,
-  kSiteSoftEnd = 33
+  kSiteSoftEnd = 33,
+  kSiteSoftStore = 34
 };
 
 // All lanes wait; the result is made warp-uniform so that the collective
@@ -85,34 +90,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, DevSta
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void store_row(const FwdArgs& a, int64_t row, const uint32_t* ov,
-                                          float inv_l) {
-  if (a.o_fp32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.o) + row * kHeadDim);
-#pragma unroll
-    for (int x = 0; x < 16; ++x) {
-      dst[x] = make_float4(__uint_as_float(ov[4 * x]) * inv_l,
-                           __uint_as_float(ov[4 * x + 1]) * inv_l,
-                           __uint_as_float(ov[4 * x + 2]) * inv_l,
-                           __uint_as_float(ov[4 * x + 3]) * inv_l);
-    }
-  } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o) + row * kHeadDim);
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      uint4 w;
-      w.x = pack_bf16x2(__uint_as_float(ov[8 * x + 0]) * inv_l, __uint_as_float(ov[8 * x + 1]) * inv_l);
-      w.y = pack_bf16x2(__uint_as_float(ov[8 * x + 2]) * inv_l, __uint_as_float(ov[8 * x + 3]) * inv_l);
-      w.z = pack_bf16x2(__uint_as_float(ov[8 * x + 4]) * inv_l, __uint_as_float(ov[8 * x + 5]) * inv_l);
-      w.w = pack_bf16x2(__uint_as_float(ov[8 * x + 6]) * inv_l, __uint_as_float(ov[8 * x + 7]) * inv_l);
-      dst[x] = w;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     bam_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                   const FwdArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // Aligned by an offset from the shared array itself (not through an
   // integer cast), so that accesses stay in the shared address space.
@@ -148,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.s_free[t], 4);
       mbar_init(&sm.p_full[t], 4);
       mbar_init(&sm.pv_done[t], 1);
+      mbar_init(&sm.o_full[t], 4);
     }
     mbar_init(&sm.mma_final, 1);
     fence_barrier_init();
@@ -454,10 +436,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         reg_fence32(ov);
         reg_fence32(ov + 32);
-        if (i < a.T) {
-          const int64_t row = static_cast<int64_t>(bh) * a.T + i;
-          store_row(a, row, ov, 1.0f / l);
-          if (a.lse) a.lse[row] = (m + __log2f(le)) * kLn2f;
+        // Row r of the tile into the staging tile (128-byte rows, 16-byte
+        // chunk c at (c ^ (r % 8)) * 16); one TMA store per box writes the
+        // tile, clipped at T.
+        const float inv_l = 1.0f / l;
+        if (a.o_fp32) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            uint8_t* rowp = sm.ost[t] + b * kTileBytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t* v4 = ov + 32 * b + 4 * c;
+              *reinterpret_cast<float4*>(rowp + ((c ^ (r & 7)) << 4)) =
+                  make_float4(__uint_as_float(v4[0]) * inv_l, __uint_as_float(v4[1]) * inv_l,
+                              __uint_as_float(v4[2]) * inv_l, __uint_as_float(v4[3]) * inv_l);
+            }
+          }
+        } else {
+          uint8_t* rowp = sm.ost[t] + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t* v8 = ov + 8 * c;
+            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = make_uint4(
+                pack_bf16x2(__uint_as_float(v8[0]) * inv_l, __uint_as_float(v8[1]) * inv_l),
+                pack_bf16x2(__uint_as_float(v8[2]) * inv_l, __uint_as_float(v8[3]) * inv_l),
+                pack_bf16x2(__uint_as_float(v8[4]) * inv_l, __uint_as_float(v8[5]) * inv_l),
+                pack_bf16x2(__uint_as_float(v8[6]) * inv_l, __uint_as_float(v8[7]) * inv_l));
+          }
+        }
+        if (i < a.T && a.lse) a.lse[static_cast<int64_t>(bh) * a.T + i] = (m + __log2f(le)) * kLn2f;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.o_full[t]);
+        if ((warp & 3) == 0 && lane == 0) {
+          // The tile's first warp stores it once all four have staged.
+          if (mbar_wait(&sm.o_full[t], 0, a.status, ab, kSiteSoftStore)) {
+            const int row0 = i0 + 128 * t;
+            if (a.o_fp32) {
+              tma_store_3d(&to, sm.ost[t], 0, row0, bh);
+              tma_store_3d(&to, sm.ost[t] + kTileBytes, 32, row0, bh);
+            } else {
+              tma_store_3d(&to, sm.ost[t], 0, row0, bh);
+            }
+            bulk_commit();
+            bulk_wait_read_all();  // the staging tile stays valid until read
+          }
         }
       }
     }
@@ -474,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, cudaStream_t st) {
+                       const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(FwdSmem) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -485,7 +508,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     attr_set = true;
   }
   const unsigned grid = static_cast<unsigned>(a.nqb) * static_cast<unsigned>(a.B * a.H);
-  return launch_k(bam_fwd_kernel, dim3(grid), dim3(kThreads), smem, st, true, tq, tk, tv, a);
+  return launch_k(bam_fwd_kernel, dim3(grid), dim3(kThreads), smem, st, true, tq, tk, tv, to, a);
 }
 
 }  // namespace bam
