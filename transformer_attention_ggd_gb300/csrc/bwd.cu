@@ -20,25 +20,30 @@
 // tile of one (b, h), and for each the 128-row query tiles that see it (the
 // next item's K/V and first S/dP overlap the current item's last tile and
 // its dK/dV epilogue):
-//   warp 16    TMA producer: K, V once; per query tile Q, dO and the three
+//   warp 8     TMA producer: K, V once; per query tile Q, dO and the three
 //              256-entry distance windows (b, db/dbeta, db/dmu, four shifted
 //              reversed copies each for 16-byte loads), 2 stages.
-//   warp 17    MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
+//   warp 9     MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
 //              dV += P^T dO and dK += (c dS)^T Q (A operands MN-major in shared
 //              memory, M = keys) and dQ = (c dS) K (A = c dS from TMEM).
 //              S and dP of the next query tile are issued as soon as every
 //              element-wise warp has read its last S/dP columns of this one,
 //              so they overlap the end of this tile's element-wise work.
-//   warp 18    dQ reducer: issues the TMA reduction of each staged dQ tile
-//              into the fp32 accumulator and frees the staging tile.
-//   warps 0-15 four warps per TMEM lane quarter; each thread owns one query
-//              row and one quarter (32 keys) of the tile: P, dS, the scalar-
-//              gradient sums (as f32x2 pairs of partial sums), P and c*dS to
-//              shared memory and c*dS to TMEM (each chunk stored one chunk
-//              later, so the wait for the previous tile's products overlaps
-//              arithmetic); the finished dQ tile goes to a shared staging
-//              tile for warp 18.  At the end, dK and dV rows (TMEM lane =
-//              key) go out as bf16.
+//   warp 10    dQ reducer: issues the TMA reduction of each staged dQ tile
+//              into the fp32 accumulator and frees the staging tile; at an
+//              item's end, the TMA stores of its dK and dV.
+//   warps 0-7  two warps per TMEM lane quarter; each thread owns one query
+//              row and half (64 keys) of the tile, in 8-key chunks whose S/dP
+//              columns load while the previous chunk is computed: P, dS, the
+//              scalar-gradient sums (as f32x2 pairs of partial sums), P and
+//              c*dS to shared memory and c*dS to TMEM (each chunk stored one
+//              chunk later, so the wait for the previous tile's products
+//              overlaps arithmetic); the finished dQ tile goes to a shared
+//              staging tile for warp 10.  At an item's end, its dK and dV rows
+//              (TMEM lane = key) are staged as bf16 for warp 10.  Eight such
+//              warps (168 registers, no spills) measured as fast as sixteen
+//              (96 registers, spills) and leave the MMA issuer fewer busy
+//              warps on its scheduler.
 // TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
 //               dK [384,448) dV [448,512).
 #include <type_traits>
@@ -49,14 +54,17 @@ namespace bam {
 namespace {
 
 constexpr int kBStages = 2;
-constexpr int kBCompute = 16;   // element-wise warps: four per TMEM lane quarter
-// + producer + MMA issuer + dQ reducer (still 96 registers per thread: the
-// register file is split per scheduler, and 19 warps put at most 5 on one)
+// Element-wise warps, a multiple of 4 (kBCompute / 4 per TMEM lane quarter).
+constexpr int kBCompute = 8;
+// + producer + MMA issuer + dQ reducer: 11 warps, at most 3 on one
+// scheduler, so 168 registers per thread fit its share of the register file.
 constexpr int kBThreads = 32 * (kBCompute + 3);
 constexpr int kBProducerWarp = kBCompute;
 constexpr int kBMmaWarp = kBCompute + 1;
 constexpr int kBDqWarp = kBCompute + 2;
-constexpr int kBKeysPerWarp = 128 / (kBCompute / 4);  // 32 keys of the tile per thread
+constexpr int kBKeysPerWarp = 128 / (kBCompute / 4);  // keys of the tile per thread
+constexpr int kBChunks = kBKeysPerWarp / 8;            // 8-key chunks per thread and tile
+constexpr int kBDims = kHeadDim / (kBCompute / 4);     // dQ/dK/dV columns per warp
 constexpr int kTile = 128 * 64 * 2;  // 16 KB bf16 tile
 constexpr int kBWin = 256;            // window entries per query tile
 constexpr int kBWinCopy = kBWin + 4;  // entries per reversed copy (shifts of 0..3)
@@ -396,7 +404,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   } else {
     // ------------------------------------------------------------ element-wise
     const int r = 32 * (warp & 3) + lane;  // query row within the tile = TMEM lane
-    const int hc = warp >> 2;              // which 32 keys of the tile
+    const int hc = warp >> 2;              // which kBKeysPerWarp keys of the tile
     const uint32_t lb = tmem_lane_base(warp);
     const int kq = (r + 1) & 3;
     const int wrev = win_copy_off(kq, kBWinCopyStride) + (127 - r + kq);
@@ -408,16 +416,20 @@ __global__ void __launch_bounds__(kBThreads, 1)
     // every warp arrives on dqs_full when its part is written.
     int n_dq = 0;  // dQ tiles staged so far
     auto dq_epilogue = [&]() -> bool {
-      uint32_t dv[16];
-      tmem_ld_32x32b_x16(tm + lb + kColDQ + 16 * hc, dv);
+      uint32_t dv[kBDims];
+#pragma unroll
+      for (int u = 0; u < kBDims / 16; ++u)
+        tmem_ld_32x32b_x16(tm + lb + kColDQ + kBDims * hc + 16 * u, dv + 16 * u);
       tmem_ld_wait();
-      reg_fence16(dv);
+#pragma unroll
+      for (int u = 0; u < kBDims / 16; ++u) reg_fence16(dv + 16 * u);
       if (n_dq > 0 && !warp_wait(&sm.dqs_free, (n_dq - 1) & 1, a.status, ab, kSiteBWgDq))
         return false;
-      uint8_t* box = reinterpret_cast<uint8_t*>(sm.dqs[hc >> 1]);
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int cc = 4 * (hc & 1) + x;  // 16-byte chunk of the 128-byte row
+      for (int x = 0; x < kBDims / 4; ++x) {
+        const int d0 = kBDims * hc + 4 * x;  // first of four dQ columns
+        uint8_t* box = reinterpret_cast<uint8_t*>(sm.dqs[d0 >> 5]);
+        const int cc = (d0 & 31) >> 2;       // 16-byte chunk of the 128-byte row
         *reinterpret_cast<uint4*>(box + r * 128 + ((cc ^ (r & 7)) << 4)) =
             make_uint4(dv[4 * x], dv[4 * x + 1], dv[4 * x + 2], dv[4 * x + 3]);
       }
@@ -489,13 +501,22 @@ __global__ void __launch_bounds__(kBThreads, 1)
           tmem_st_32x32b_x4(tm + lb + kColDS + c0 / 2, dd);
         };
         uint32_t pp_prev[4], dd_prev[4];  // chunk computed, not yet stored
-        // Four 8-key chunks of S and dP per thread.
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
+        // kBChunks 8-key chunks of S and dP per thread, in two register
+        // buffers: the next chunk's TMEM loads are in flight while this chunk
+        // is computed.
+        uint32_t sA[8], dA[8], sB[8], dB[8];
+        tmem_ld_32x32b_x8(tm + lb + kColS + kBKeysPerWarp * hc, sA);
+        tmem_ld_32x32b_x8(tm + lb + kColDP + kBKeysPerWarp * hc, dA);
+        tmem_ld_wait();
+        reg_fence8(sA);
+        reg_fence8(dA);
+        auto chunk = [&](const int ch, uint32_t (&sv)[8], uint32_t (&dpv)[8], uint32_t (&sn)[8],
+                         uint32_t (&dn)[8]) {
           const int c0 = kBKeysPerWarp * hc + 8 * ch;
-          uint32_t sv[8], dpv[8];
-          tmem_ld_32x32b_x8(tm + lb + kColS + c0, sv);
-          tmem_ld_32x32b_x8(tm + lb + kColDP + c0, dpv);
+          if (ch + 1 < kBChunks) {
+            tmem_ld_32x32b_x8(tm + lb + kColS + c0 + 8, sn);
+            tmem_ld_32x32b_x8(tm + lb + kColDP + c0 + 8, dn);
+          }
           uint64_t tb[4], tbeta[4], tmu[4];
           const float* wp = wv + c0;
           ld_f2x2(wp, tb[0], tb[1]);
@@ -504,16 +525,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
           ld_f2x2(wp + kBWinPlane + 4, tbeta[2], tbeta[3]);
           ld_f2x2(wp + 2 * kBWinPlane, tmu[0], tmu[1]);
           ld_f2x2(wp + 2 * kBWinPlane + 4, tmu[2], tmu[3]);
-          tmem_ld_wait();
-          reg_fence8(sv);
-          reg_fence8(dpv);
-          if (ch == 3) {
-            // This warp's last S/dP columns of the tile are in registers: the
-            // next tile's S and dP may be written over them.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.sdp_free);
-          }
           uint32_t pp[4], dd[4];
           // Masked keys (past the causal limit or T) only in chunks that reach
           // them; the test is warp-uniform so each warp takes one version.
@@ -553,23 +564,35 @@ __global__ void __launch_bounds__(kBThreads, 1)
             elementwise(std::true_type{});
           else
             elementwise(std::false_type{});
+          if (ch + 1 < kBChunks) {
+            tmem_ld_wait();
+            reg_fence8(sn);
+            reg_fence8(dn);
+          }
+          if (ch + 2 == kBChunks) {
+            // This warp's last S/dP columns of the tile are in registers: the
+            // next tile's S and dP may be written over them.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.sdp_free);
+          }
           if (ch == 1 && t > 0) {
             // The previous tile's gradient products must be done before its
             // P^T / dS^T buffers and dS TMEM are overwritten; its dQ tile is
             // drained here, before this tile's dQ product is issued.  (The
             // previous item's last tile was drained at that item's end.)
             ok = warp_wait(&sm.mma_done, (g - 1) & 1, a.status, ab, kSiteBWgDone);
-            if (!ok) break;
+            if (!ok) return;
             tc_fence_after();
             if (!dq_epilogue()) {
               ok = false;
-              break;
+              return;
             }
           }
           if (ch == 1 && t == 0 && round > 0) {
             // The previous item's dK/dV staging in the P^T buffer is read.
             ok = warp_wait(&sm.epi_free, (round - 1) & 1, a.status, ab, kSiteBWgDq);
-            if (!ok) break;
+            if (!ok) return;
           }
           if (ch > 0) store_chunk(c0 - 8, pp_prev, dd_prev);
 #pragma unroll
@@ -577,9 +600,16 @@ __global__ void __launch_bounds__(kBThreads, 1)
             pp_prev[x] = pp[x];
             dd_prev[x] = dd[x];
           }
+        };
+        static_assert(kBChunks % 2 == 0 && kBChunks >= 2, "chunks come in pairs");
+#pragma unroll 1
+        for (int ch = 0; ch < kBChunks && ok; ch += 2) {
+          chunk(ch, sA, dA, sB, dB);
+          if (!ok) break;
+          chunk(ch + 1, sB, dB, sA, dA);
         }
         if (!ok) break;
-        store_chunk(kBKeysPerWarp * hc + 24, pp_prev, dd_prev);
+        store_chunk(kBKeysPerWarp * hc + kBKeysPerWarp - 8, pp_prev, dd_prev);
         {
           float a0, a1;
           f2_unpack(rowSS2, a0, a1);
@@ -643,17 +673,19 @@ __global__ void __launch_bounds__(kBThreads, 1)
           // dK and dV rows as bf16 into the P^T buffer (free once the item's
           // last products are done), 128-byte rows with the 128-byte swizzle,
           // for the dQ warp's TMA stores: TMEM lane = key j0 + r; this warp
-          // holds 16 of the 64 dimensions (two 16-byte chunks of the row).
+          // holds kBDims of the 64 dimensions (16-byte chunks of 8 columns).
           for (int which = 0; which < 2; ++which) {
-            const uint32_t col = (which ? kColDV : kColDK) + 16 * hc;
-            uint32_t kvv[16];
-            tmem_ld_32x32b_x16(tm + lb + col, kvv);
+            const uint32_t col = (which ? kColDV : kColDK) + kBDims * hc;
+            uint32_t kvv[kBDims];
+#pragma unroll
+            for (int u = 0; u < kBDims / 16; ++u) tmem_ld_32x32b_x16(tm + lb + col + 16 * u, kvv + 16 * u);
             tmem_ld_wait();
-            reg_fence16(kvv);
+#pragma unroll
+            for (int u = 0; u < kBDims / 16; ++u) reg_fence16(kvv + 16 * u);
             uint8_t* rowp = sm.pt + which * kTile + r * 128;
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-              const int cc = 2 * hc + x;
+            for (int x = 0; x < kBDims / 8; ++x) {
+              const int cc = (kBDims / 8) * hc + x;
               *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) = make_uint4(
                   pack_bf16x2(__uint_as_float(kvv[8 * x]), __uint_as_float(kvv[8 * x + 1])),
                   pack_bf16x2(__uint_as_float(kvv[8 * x + 2]), __uint_as_float(kvv[8 * x + 3])),
