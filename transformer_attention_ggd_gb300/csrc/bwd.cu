@@ -33,8 +33,7 @@
 //              into the fp32 accumulator and frees the staging tile; at an
 //              item's end, the TMA stores of its dK and dV.
 //   warps 0-7  two warps per TMEM lane quarter; each thread owns one query
-//              row and half (64 keys) of the tile, in 8-key chunks whose S/dP
-//              columns load while the previous chunk is computed: P, dS, the
+//              row and half (64 keys) of the tile, in 16-key chunks: P, dS, the
 //              scalar-gradient sums (as f32x2 pairs of partial sums), P and
 //              c*dS to shared memory and c*dS to TMEM (each chunk stored one
 //              chunk later, so the wait for the previous tile's products
@@ -63,7 +62,6 @@ constexpr int kBProducerWarp = kBCompute;
 constexpr int kBMmaWarp = kBCompute + 1;
 constexpr int kBDqWarp = kBCompute + 2;
 constexpr int kBKeysPerWarp = 128 / (kBCompute / 4);  // keys of the tile per thread
-constexpr int kBChunks = kBKeysPerWarp / 8;            // 8-key chunks per thread and tile
 constexpr int kBDims = kHeadDim / (kBCompute / 4);     // dQ/dK/dV columns per warp
 constexpr int kTile = 128 * 64 * 2;  // 16 KB bf16 tile
 constexpr int kBWin = 256;            // window entries per query tile
@@ -500,37 +498,42 @@ __global__ void __launch_bounds__(kBThreads, 1)
           *reinterpret_cast<uint4*>(sm.dst + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
           tmem_st_32x32b_x4(tm + lb + kColDS + c0 / 2, dd);
         };
-        uint32_t pp_prev[4], dd_prev[4];  // chunk computed, not yet stored
-        // kBChunks 8-key chunks of S and dP per thread, in two register
-        // buffers: the next chunk's TMEM loads are in flight while this chunk
-        // is computed.
-        uint32_t sA[8], dA[8], sB[8], dB[8];
-        tmem_ld_32x32b_x8(tm + lb + kColS + kBKeysPerWarp * hc, sA);
-        tmem_ld_32x32b_x8(tm + lb + kColDP + kBKeysPerWarp * hc, dA);
-        tmem_ld_wait();
-        reg_fence8(sA);
-        reg_fence8(dA);
-        auto chunk = [&](const int ch, uint32_t (&sv)[8], uint32_t (&dpv)[8], uint32_t (&sn)[8],
-                         uint32_t (&dn)[8]) {
-          const int c0 = kBKeysPerWarp * hc + 8 * ch;
-          if (ch + 1 < kBChunks) {
-            tmem_ld_32x32b_x8(tm + lb + kColS + c0 + 8, sn);
-            tmem_ld_32x32b_x8(tm + lb + kColDP + c0 + 8, dn);
-          }
-          uint64_t tb[4], tbeta[4], tmu[4];
+        // 16-key chunks of S and dP per thread (eight independent column
+        // pairs per chunk: measured 5% faster than 8-key chunks with the next
+        // chunk's columns prefetched).
+        uint32_t pp_prev[8], dd_prev[8];  // chunk computed, not yet stored
+        constexpr int kCW = 16;
+        constexpr int kNC = kBKeysPerWarp / kCW;
+#pragma unroll 1
+        for (int ch = 0; ch < kNC; ++ch) {
+          const int c0 = kBKeysPerWarp * hc + kCW * ch;
+          uint32_t sv[16], dpv[16];
+          tmem_ld_32x32b_x16(tm + lb + kColS + c0, sv);
+          tmem_ld_32x32b_x16(tm + lb + kColDP + c0, dpv);
+          uint64_t tb[8], tbeta[8], tmu[8];
           const float* wp = wv + c0;
-          ld_f2x2(wp, tb[0], tb[1]);
-          ld_f2x2(wp + 4, tb[2], tb[3]);
-          ld_f2x2(wp + kBWinPlane, tbeta[0], tbeta[1]);
-          ld_f2x2(wp + kBWinPlane + 4, tbeta[2], tbeta[3]);
-          ld_f2x2(wp + 2 * kBWinPlane, tmu[0], tmu[1]);
-          ld_f2x2(wp + 2 * kBWinPlane + 4, tmu[2], tmu[3]);
-          uint32_t pp[4], dd[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            ld_f2x2(wp + 4 * q, tb[2 * q], tb[2 * q + 1]);
+            ld_f2x2(wp + kBWinPlane + 4 * q, tbeta[2 * q], tbeta[2 * q + 1]);
+            ld_f2x2(wp + 2 * kBWinPlane + 4 * q, tmu[2 * q], tmu[2 * q + 1]);
+          }
+          tmem_ld_wait();
+          reg_fence16(sv);
+          reg_fence16(dpv);
+          if (ch == kNC - 1) {
+            // This warp's last S/dP columns of the tile are in registers: the
+            // next tile's S and dP may be written over them.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.sdp_free);
+          }
+          uint32_t pp[8], dd[8];
           // Masked keys (past the causal limit or T) only in chunks that reach
           // them; the test is warp-uniform so each warp takes one version.
           auto elementwise = [&](auto masked) {
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
+            for (int x = 0; x < 8; ++x) {
               const int c = c0 + 2 * x;
               const uint64_t s2 =
                   f2_pack(__uint_as_float(sv[2 * x]), __uint_as_float(sv[2 * x + 1]));
@@ -560,56 +563,41 @@ __global__ void __launch_bounds__(kBThreads, 1)
               dd[x] = pack_bf16x2(q0, q1);
             }
           };
-          if (__any_sync(0xffffffffu, c0 + 7 > lim))
+          if (__any_sync(0xffffffffu, c0 + kCW - 1 > lim))
             elementwise(std::true_type{});
           else
             elementwise(std::false_type{});
-          if (ch + 1 < kBChunks) {
-            tmem_ld_wait();
-            reg_fence8(sn);
-            reg_fence8(dn);
-          }
-          if (ch + 2 == kBChunks) {
-            // This warp's last S/dP columns of the tile are in registers: the
-            // next tile's S and dP may be written over them.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.sdp_free);
-          }
           if (ch == 1 && t > 0) {
             // The previous tile's gradient products must be done before its
             // P^T / dS^T buffers and dS TMEM are overwritten; its dQ tile is
             // drained here, before this tile's dQ product is issued.  (The
             // previous item's last tile was drained at that item's end.)
             ok = warp_wait(&sm.mma_done, (g - 1) & 1, a.status, ab, kSiteBWgDone);
-            if (!ok) return;
+            if (!ok) break;
             tc_fence_after();
             if (!dq_epilogue()) {
               ok = false;
-              return;
+              break;
             }
           }
           if (ch == 1 && t == 0 && round > 0) {
             // The previous item's dK/dV staging in the P^T buffer is read.
             ok = warp_wait(&sm.epi_free, (round - 1) & 1, a.status, ab, kSiteBWgDq);
-            if (!ok) return;
+            if (!ok) break;
           }
-          if (ch > 0) store_chunk(c0 - 8, pp_prev, dd_prev);
+          if (ch > 0) {
+            store_chunk(c0 - kCW, pp_prev, dd_prev);
+            store_chunk(c0 - kCW + 8, pp_prev + 4, dd_prev + 4);
+          }
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
+          for (int x = 0; x < 8; ++x) {
             pp_prev[x] = pp[x];
             dd_prev[x] = dd[x];
           }
-        };
-        static_assert(kBChunks % 2 == 0 && kBChunks >= 2, "chunks come in pairs");
-#pragma unroll 1
-        for (int ch = 0; ch < kBChunks && ok; ch += 2) {
-          chunk(ch, sA, dA, sB, dB);
-          if (!ok) break;
-          chunk(ch + 1, sB, dB, sA, dA);
         }
         if (!ok) break;
-        store_chunk(kBKeysPerWarp * hc + kBKeysPerWarp - 8, pp_prev, dd_prev);
+        store_chunk(kBKeysPerWarp * hc + kBKeysPerWarp - 16, pp_prev, dd_prev);
+        store_chunk(kBKeysPerWarp * hc + kBKeysPerWarp - 8, pp_prev + 4, dd_prev + 4);
         {
           float a0, a1;
           f2_unpack(rowSS2, a0, a1);
