@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
     if (lane == 0) {
       bool ok = (*ab == 0);
       int g = 0, n = 0;
+      int issued = 0;  // query tiles whose Q/dO/window copies were issued
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
@@ -250,28 +251,35 @@ __global__ void __launch_bounds__(kBThreads, 1)
             for (int k = 0; k < kTabCopies; ++k)
               bulk_load(sm.win[s][p] + win_copy_off(k, kBWinCopyStride),
                         src + p * plane + k * copy_stride, kBWinCopy * 4, &sm.qd_full[s]);
+          issued = g + 1;
           if (t == 0) {
             // K and V of the item into the single K/V buffers: V as soon as
             // the previous item's last dP product is done, K after its last
             // dQ product (issued first among that tile's gradient products).
-            mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
+            // kv_full is armed only after v_empty: that product was issued
+            // after the MMA warp saw the previous K/V phase complete, so the
+            // barrier is never armed while that phase still has bytes in
+            // flight (a one-tile item is followed at once by the next item,
+            // before its own K/V loads need have landed).
             if (n > 0) {
               ok = mbar_wait(&sm.v_empty, (n - 1) & 1, a.status, ab, kSiteBProd);
               if (!ok) break;
             }
+            mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
             tma_load_3d(sm.v, &tv, &sm.kv_full, 0, it.j0, it.bh);
-            if (n > 0) {
-              ok = mbar_wait(&sm.k_empty, (n - 1) & 1, a.status, ab, kSiteBProd);
-              if (!ok) break;
-            }
+            // After a failed wait K is loaded all the same (the kernel is
+            // giving up, so what K's buffer feeds no longer matters): the
+            // phase then completes and the drain below sees both copies land.
+            if (n > 0) ok = mbar_wait(&sm.k_empty, (n - 1) & 1, a.status, ab, kSiteBProd);
             tma_load_3d(sm.k, &tk, &sm.kv_full, 0, it.j0, it.bh);
             ++n;
+            if (!ok) break;
           }
         }
       }
       // Copies still in flight land before this CTA leaves.
       if (n > 0) mbar_drain(&sm.kv_full, (n - 1) & 1);
-      for (int x = max(0, g - kBStages); x < g; ++x)
+      for (int x = max(0, issued - kBStages); x < issued; ++x)
         mbar_drain(&sm.qd_full[x % kBStages], (x / kBStages) & 1);
     }
   } else if (warp == kBMmaWarp) {
@@ -687,6 +695,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
         }
       }
     }
+    // A warp that gave up inside a tile may still have TMEM stores in
+    // flight; they complete before the columns are freed.
+    tmem_st_wait();
   }
 
   tc_fence_before();
