@@ -27,6 +27,12 @@
 //  * backward: the pages give none; the plain chain rule of L = sum(O * dO).
 //    At u = 0 (beta > 0) the contributions to dalpha, dbeta, dmu are 0 (their
 //    limits, with sgn(0) = 0); where the eps clamp is active du/dmu = 0.
+//  * theta prior (prior = 1): the repository README's own parameterisation,
+//    "Implementation Details" (the bias equation and AttentionPrior.forward):
+//    b = -exp(theta_alpha) * (|d - mu| + eps)^theta_beta with
+//    mu = exp(theta_mu) - exp(-theta_mu) and eps added for every theta_beta;
+//    the gradients are with respect to theta_alpha, theta_beta, theta_mu.
+//    With eps = 0 and |d - mu| = 0 the value is 0 for theta_beta > 0.
 //
 // Layouts: q, k, v, o, dO, dq, dk, dv are [B, H, T, D] row-major doubles;
 // lse is [B, H, T] (natural log); per-head parameters are double[H].
@@ -43,13 +49,14 @@
 namespace {
 
 struct Params {
-    const double* alpha;
-    const double* beta;
-    const double* mu;
-    const double* s;  // SSMax scale, read only when ssmax != 0
+    const double* alpha;  // theta_alpha when prior == 1
+    const double* beta;   // theta_beta when prior == 1
+    const double* mu;     // theta_mu when prior == 1
+    const double* s;      // SSMax scale, read only when ssmax != 0
     double eps;
     int causal;
     int ssmax;
+    int prior;  // 0: -(u/alpha)^beta with the eps clamp; 1: theta prior
 };
 
 // |d - mu|, clamped to eps for beta <= 0.  Returns whether the clamp is active.
@@ -98,6 +105,48 @@ void bias_grad(double d, double alpha, double beta, double mu, double eps,
     }
 }
 
+// theta prior: b = -exp(ta) * w^tb, w = |d - mu| + eps, mu = exp(tm) - exp(-tm).
+double theta_mu_value(double tm) { return std::exp(tm) - std::exp(-tm); }
+
+double bias_theta(double d, double ta, double tb, double tm, double eps) {
+    double w = std::fabs(d - theta_mu_value(tm)) + eps;
+    if (w == 0.0) return 0.0;  // eps == 0 at d == mu, tb > 0: 0^tb = 0
+    return -std::exp(ta) * std::pow(w, tb);
+}
+
+// Its partial derivatives, by hand:
+//   db/dta = b,   db/dtb = b * ln(w),
+//   db/dw = tb * b / w,  dw/dmu = -sgn(d - mu),  dmu/dtm = exp(tm) + exp(-tm).
+void bias_theta_grad(double d, double ta, double tb, double tm, double eps,
+                     double* gta, double* gtb, double* gtm) {
+    double mu = theta_mu_value(tm);
+    double w = std::fabs(d - mu) + eps;
+    if (w == 0.0) {
+        *gta = 0.0;
+        *gtb = 0.0;
+        *gtm = 0.0;
+        return;
+    }
+    double b = -std::exp(ta) * std::pow(w, tb);
+    *gta = b;
+    *gtb = b * std::log(w);
+    double sgn = (d - mu > 0.0) ? 1.0 : ((d - mu < 0.0) ? -1.0 : 0.0);
+    *gtm = (tb * b / w) * (-sgn) * (std::exp(tm) + std::exp(-tm));
+}
+
+// The bias and its three partials for head h under either prior.
+double bias_of(const Params& p, int h, double d) {
+    if (p.prior) return bias_theta(d, p.alpha[h], p.beta[h], p.mu[h], p.eps);
+    return bias(d, p.alpha[h], p.beta[h], p.mu[h], p.eps);
+}
+
+void bias_grad_of(const Params& p, int h, double d, double* g0, double* g1, double* g2) {
+    if (p.prior)
+        bias_theta_grad(d, p.alpha[h], p.beta[h], p.mu[h], p.eps, g0, g1, g2);
+    else
+        bias_grad(d, p.alpha[h], p.beta[h], p.mu[h], p.eps, g0, g1, g2);
+}
+
 double dot(const double* a, const double* b, int D) {
     double acc = 0.0;
     for (int x = 0; x < D; ++x) acc += a[x] * b[x];
@@ -118,13 +167,13 @@ double row_scale(const Params& p, int h, int n, int D) {
 // qi: the query row; kb, vb: the [T, D] keys and values of this (b, h);
 // query position `pos` (distance d = pos - j); n visible keys 0..n-1.
 void forward_row(const double* qi, const double* kb, const double* vb, int n,
-                 int pos, int D, double c, double alpha, double beta, double mu,
-                 double eps, double* out, double* lse, std::vector<double>& z) {
+                 int pos, int D, double c, const Params& p, int h, double* out, double* lse,
+                 std::vector<double>& z) {
     z.resize(n);
     double m = -INFINITY;
     for (int j = 0; j < n; ++j) {
         z[j] = c * dot(qi, kb + static_cast<size_t>(j) * D, D) +
-               bias(static_cast<double>(pos - j), alpha, beta, mu, eps);
+               bias_of(p, h, static_cast<double>(pos - j));
         m = std::max(m, z[j]);
     }
     double l = 0.0;
@@ -166,24 +215,28 @@ void parallel_for(int64_t n, int nthreads, F fn) {
 extern "C" {
 
 // b(d) for one head; exposed so that tests can check the bias in isolation.
-double bam_oracle_bias(double d, double alpha, double beta, double mu, double eps) {
-    return bias(d, alpha, beta, mu, eps);
+// prior 1: (alpha, beta, mu) are (theta_alpha, theta_beta, theta_mu).
+double bam_oracle_bias(double d, double alpha, double beta, double mu, double eps, int prior) {
+    return prior ? bias_theta(d, alpha, beta, mu, eps) : bias(d, alpha, beta, mu, eps);
 }
 
-// db/dalpha, db/dbeta, db/dmu at distance d; out[3].
+// The three partials of b at distance d; out[3].
 void bam_oracle_bias_grad(double d, double alpha, double beta, double mu, double eps,
-                          double* out) {
-    bias_grad(d, alpha, beta, mu, eps, out, out + 1, out + 2);
+                          int prior, double* out) {
+    if (prior)
+        bias_theta_grad(d, alpha, beta, mu, eps, out, out + 1, out + 2);
+    else
+        bias_grad(d, alpha, beta, mu, eps, out, out + 1, out + 2);
 }
 
 // Forward of selected rows.  rows[r] = (b*H + h)*T + i.  o: [nrows, D], lse: [nrows].
 int bam_oracle_fwd_rows(const double* q, const double* k, const double* v, int B, int H,
                         int T, int D, const double* alpha, const double* beta,
                         const double* mu, const double* s, double eps, int causal,
-                        int ssmax, const int64_t* rows, int64_t nrows, double* o,
+                        int ssmax, int prior, const int64_t* rows, int64_t nrows, double* o,
                         double* lse, int nthreads) {
     if (B < 1 || H < 1 || T < 1 || D < 1) return 1;
-    Params p{alpha, beta, mu, s, eps, causal, ssmax};
+    Params p{alpha, beta, mu, s, eps, causal, ssmax, prior};
     parallel_for(nrows, nthreads, [&](int64_t r) {
         thread_local std::vector<double> z;
         int64_t flat = rows[r];
@@ -194,8 +247,7 @@ int bam_oracle_fwd_rows(const double* q, const double* k, const double* v, int B
         int n = n_visible(i, T, causal);
         double c = row_scale(p, h, n, D);
         forward_row(q + base + static_cast<size_t>(i) * D, k + base, v + base, n, i, D, c,
-                    alpha[h], beta[h], mu[h], eps, o + static_cast<size_t>(r) * D, lse + r,
-                    z);
+                    p, h, o + static_cast<size_t>(r) * D, lse + r, z);
     });
     return 0;
 }
@@ -203,10 +255,10 @@ int bam_oracle_fwd_rows(const double* q, const double* k, const double* v, int B
 // Full forward: o [B,H,T,D], lse [B,H,T].
 int bam_oracle_fwd(const double* q, const double* k, const double* v, int B, int H, int T,
                    int D, const double* alpha, const double* beta, const double* mu,
-                   const double* s, double eps, int causal, int ssmax, double* o,
+                   const double* s, double eps, int causal, int ssmax, int prior, double* o,
                    double* lse, int nthreads) {
     if (B < 1 || H < 1 || T < 1 || D < 1) return 1;
-    Params p{alpha, beta, mu, s, eps, causal, ssmax};
+    Params p{alpha, beta, mu, s, eps, causal, ssmax, prior};
     parallel_for(static_cast<int64_t>(B) * H * T, nthreads, [&](int64_t flat) {
         thread_local std::vector<double> z;
         int i = static_cast<int>(flat % T);
@@ -216,8 +268,7 @@ int bam_oracle_fwd(const double* q, const double* k, const double* v, int B, int
         int n = n_visible(i, T, causal);
         double c = row_scale(p, h, n, D);
         forward_row(q + base + static_cast<size_t>(i) * D, k + base, v + base, n, i, D, c,
-                    alpha[h], beta[h], mu[h], eps, o + static_cast<size_t>(flat) * D,
-                    lse + flat, z);
+                    p, h, o + static_cast<size_t>(flat) * D, lse + flat, z);
     });
     return 0;
 }
@@ -227,18 +278,17 @@ int bam_oracle_fwd(const double* q, const double* k, const double* v, int B, int
 // q: [B,H,D]; kc, vc: [B,H,Tkv,D]; o: [B,H,D]; lse: [B,H].
 int bam_oracle_decode(const double* q, const double* kc, const double* vc, int B, int H,
                       int Tkv, int D, const double* alpha, const double* beta,
-                      const double* mu, const double* s, double eps, int ssmax, double* o,
-                      double* lse, int nthreads) {
+                      const double* mu, const double* s, double eps, int ssmax, int prior,
+                      double* o, double* lse, int nthreads) {
     if (B < 1 || H < 1 || Tkv < 1 || D < 1) return 1;
-    Params p{alpha, beta, mu, s, eps, 1, ssmax};
+    Params p{alpha, beta, mu, s, eps, 1, ssmax, prior};
     parallel_for(static_cast<int64_t>(B) * H, nthreads, [&](int64_t bh) {
         thread_local std::vector<double> z;
         int h = static_cast<int>(bh % H);
         size_t base = static_cast<size_t>(bh) * Tkv * D;
         double c = row_scale(p, h, Tkv, D);
         forward_row(q + static_cast<size_t>(bh) * D, kc + base, vc + base, Tkv, Tkv - 1, D,
-                    c, alpha[h], beta[h], mu[h], eps, o + static_cast<size_t>(bh) * D,
-                    lse + bh, z);
+                    c, p, h, o + static_cast<size_t>(bh) * D, lse + bh, z);
     });
     return 0;
 }
@@ -258,10 +308,11 @@ int bam_oracle_decode(const double* q, const double* kc, const double* vc, int B
 int bam_oracle_bwd(const double* q, const double* k, const double* v, const double* dO,
                    int B, int H, int T, int D, const double* alpha, const double* beta,
                    const double* mu, const double* s, double eps, int causal, int ssmax,
-                   double* dq, double* dk, double* dv, double* dalpha, double* dbeta,
-                   double* dmu, double* ds, double* absg, double* absp, int nthreads) {
+                   int prior, double* dq, double* dk, double* dv, double* dalpha,
+                   double* dbeta, double* dmu, double* ds, double* absg, double* absp,
+                   int nthreads) {
     if (B < 1 || H < 1 || T < 1 || D < 1) return 1;
-    Params p{alpha, beta, mu, s, eps, causal, ssmax};
+    Params p{alpha, beta, mu, s, eps, causal, ssmax, prior};
     const int64_t BH = static_cast<int64_t>(B) * H;
     std::vector<double> part(static_cast<size_t>(BH) * 12, 0.0);
     const double invsqrt = 1.0 / std::sqrt(static_cast<double>(D));
@@ -288,7 +339,7 @@ int bam_oracle_bwd(const double* q, const double* k, const double* v, const doub
             double m = -INFINITY;
             for (int j = 0; j < n; ++j) {
                 z[j] = c * dot(qi, kb + static_cast<size_t>(j) * D, D) +
-                       bias(static_cast<double>(i - j), alpha[h], beta[h], mu[h], eps);
+                       bias_of(p, h, static_cast<double>(i - j));
                 m = std::max(m, z[j]);
             }
             double l = 0.0;
@@ -314,8 +365,7 @@ int bam_oracle_bwd(const double* q, const double* k, const double* v, const doub
                     dvj[x] += P[j] * gi[x];
                 }
                 double ga, gbeta, gm;
-                bias_grad(static_cast<double>(i - j), alpha[h], beta[h], mu[h], eps, &ga,
-                          &gbeta, &gm);
+                bias_grad_of(p, h, static_cast<double>(i - j), &ga, &gbeta, &gm);
                 double gs = ssmax ? std::log(static_cast<double>(n)) * invsqrt * dot(qi, kj, D)
                                   : 0.0;
                 double t[4] = {dS * ga, dS * gbeta, dS * gm, dS * gs};

@@ -50,21 +50,21 @@ def _load():
             i = ctypes.c_int
             d = ctypes.c_double
             lib.bam_oracle_bias.restype = d
-            lib.bam_oracle_bias.argtypes = [d, d, d, d, d]
+            lib.bam_oracle_bias.argtypes = [d, d, d, d, d, i]
             lib.bam_oracle_bias_grad.restype = None
-            lib.bam_oracle_bias_grad.argtypes = [d, d, d, d, d, dp]
+            lib.bam_oracle_bias_grad.argtypes = [d, d, d, d, d, i, dp]
             lib.bam_oracle_fwd.restype = i
-            lib.bam_oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, dp, dp, dp, dp, d, i, i,
+            lib.bam_oracle_fwd.argtypes = [dp, dp, dp, i, i, i, i, dp, dp, dp, dp, d, i, i, i,
                                            dp, dp, i]
             lib.bam_oracle_fwd_rows.restype = i
             lib.bam_oracle_fwd_rows.argtypes = [dp, dp, dp, i, i, i, i, dp, dp, dp, dp, d, i,
-                                                i, ip, ctypes.c_int64, dp, dp, i]
+                                                i, i, ip, ctypes.c_int64, dp, dp, i]
             lib.bam_oracle_decode.restype = i
-            lib.bam_oracle_decode.argtypes = [dp, dp, dp, i, i, i, i, dp, dp, dp, dp, d, i,
+            lib.bam_oracle_decode.argtypes = [dp, dp, dp, i, i, i, i, dp, dp, dp, dp, d, i, i,
                                               dp, dp, i]
             lib.bam_oracle_bwd.restype = i
             lib.bam_oracle_bwd.argtypes = [dp, dp, dp, dp, i, i, i, i, dp, dp, dp, dp, d, i,
-                                           i, dp, dp, dp, dp, dp, dp, dp, dp, dp, i]
+                                           i, i, dp, dp, dp, dp, dp, dp, dp, dp, dp, i]
             _lib = lib
     return _lib
 
@@ -85,18 +85,29 @@ def _head_params(H, alpha, beta, mu, s):
     return alpha, beta, mu, s
 
 
-def bias(d: float, alpha: float, beta: float, mu: float, eps: float = 1e-5) -> float:
-    return _load().bam_oracle_bias(float(d), float(alpha), float(beta), float(mu), float(eps))
+# prior: 0 for b = -(u/alpha)^beta with the eps clamp; 1 for the theta prior
+# b = -exp(theta_alpha) (|d - mu| + eps)^theta_beta, mu = 2 sinh(theta_mu), in
+# which case (alpha, beta, mu) carry (theta_alpha, theta_beta, theta_mu) and
+# the gradients are with respect to those.
+PRIOR_ALPHA = 0
+PRIOR_THETA = 1
 
 
-def bias_grad(d, alpha, beta, mu, eps=1e-5) -> np.ndarray:
+def bias(d: float, alpha: float, beta: float, mu: float, eps: float = 1e-5,
+         prior: int = PRIOR_ALPHA) -> float:
+    return _load().bam_oracle_bias(float(d), float(alpha), float(beta), float(mu), float(eps),
+                                   int(prior))
+
+
+def bias_grad(d, alpha, beta, mu, eps=1e-5, prior=PRIOR_ALPHA) -> np.ndarray:
     out = np.zeros(3, dtype=np.float64)
     _load().bam_oracle_bias_grad(float(d), float(alpha), float(beta), float(mu), float(eps),
-                                 _dp(out))
+                                 int(prior), _dp(out))
     return out
 
 
-def fwd(q, k, v, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False, nthreads=0):
+def fwd(q, k, v, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False, nthreads=0,
+        prior=PRIOR_ALPHA):
     """q, k, v: [B,H,T,D] -> (o [B,H,T,D], lse [B,H,T]) in float64."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, T, D = q.shape
@@ -106,14 +117,14 @@ def fwd(q, k, v, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False, nt
     lse = np.empty((B, H, T), dtype=np.float64)
     rc = _load().bam_oracle_fwd(_dp(q), _dp(k), _dp(v), B, H, T, D, _dp(a), _dp(b), _dp(m),
                                 _dp(sc), float(eps), int(bool(causal)), int(bool(ssmax)),
-                                _dp(o), _dp(lse), int(nthreads))
+                                int(prior), _dp(o), _dp(lse), int(nthreads))
     if rc != 0:
         raise ValueError("oracle fwd: bad sizes")
     return o, lse
 
 
 def fwd_rows(q, k, v, rows, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False,
-             nthreads=0):
+             nthreads=0, prior=PRIOR_ALPHA):
     """Selected rows (flat index (b*H+h)*T+i) -> (o [n,D], lse [n])."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, T, D = q.shape
@@ -123,7 +134,7 @@ def fwd_rows(q, k, v, rows, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssma
     lse = np.empty(rows.size, dtype=np.float64)
     rc = _load().bam_oracle_fwd_rows(
         _dp(q), _dp(k), _dp(v), B, H, T, D, _dp(a), _dp(b), _dp(m), _dp(sc), float(eps),
-        int(bool(causal)), int(bool(ssmax)),
+        int(bool(causal)), int(bool(ssmax)), int(prior),
         rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.size, _dp(o), _dp(lse),
         int(nthreads))
     if rc != 0:
@@ -131,7 +142,8 @@ def fwd_rows(q, k, v, rows, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssma
     return o, lse
 
 
-def decode(q, kc, vc, alpha, beta, mu, s=None, eps=1e-5, ssmax=False, nthreads=0):
+def decode(q, kc, vc, alpha, beta, mu, s=None, eps=1e-5, ssmax=False, nthreads=0,
+           prior=PRIOR_ALPHA):
     """q [B,H,D], kc/vc [B,H,Tkv,D] -> (o [B,H,D], lse [B,H])."""
     q, kc, vc = _f64(q), _f64(kc), _f64(vc)
     B, H, Tkv, D = kc.shape
@@ -140,15 +152,15 @@ def decode(q, kc, vc, alpha, beta, mu, s=None, eps=1e-5, ssmax=False, nthreads=0
     o = np.empty((B, H, D), dtype=np.float64)
     lse = np.empty((B, H), dtype=np.float64)
     rc = _load().bam_oracle_decode(_dp(q), _dp(kc), _dp(vc), B, H, Tkv, D, _dp(a), _dp(b),
-                                   _dp(m), _dp(sc), float(eps), int(bool(ssmax)), _dp(o),
-                                   _dp(lse), int(nthreads))
+                                   _dp(m), _dp(sc), float(eps), int(bool(ssmax)), int(prior),
+                                   _dp(o), _dp(lse), int(nthreads))
     if rc != 0:
         raise ValueError("oracle decode: bad sizes")
     return o, lse
 
 
 def bwd(q, k, v, dO, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False,
-        nthreads=0):
+        nthreads=0, prior=PRIOR_ALPHA):
     """Gradients of sum(O * dO).
 
     Returns a dict with dq, dk, dv [B,H,T,D], dalpha, dbeta, dmu, ds [H],
@@ -165,7 +177,8 @@ def bwd(q, k, v, dO, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False
     absp = np.empty((4, H), dtype=np.float64)
     rc = _load().bam_oracle_bwd(_dp(q), _dp(k), _dp(v), _dp(dO), B, H, T, D, _dp(a), _dp(b),
                                 _dp(m), _dp(sc), float(eps), int(bool(causal)),
-                                int(bool(ssmax)), _dp(dq), _dp(dk), _dp(dv), _dp(g[0]),
+                                int(bool(ssmax)), int(prior), _dp(dq), _dp(dk), _dp(dv),
+                                _dp(g[0]),
                                 _dp(g[1]), _dp(g[2]), _dp(g[3]), _dp(absg), _dp(absp),
                                 int(nthreads))
     if rc != 0:
