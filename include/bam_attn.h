@@ -19,6 +19,14 @@
  * Tkv for decode).  The output is softmax_j(z_ij) applied to V ("ALiBi:
  * Attention with Linear Biases", section "Code": scores, softmax, weights @ V).
  *
+ * The prior may instead be given in the repository's own parameterisation
+ * (README, "Implementation Details": the bias equation and AttentionPrior):
+ *
+ *     b_h(d) = -exp(theta_alpha_h) * ( |d - mu_h| + eps )^theta_beta_h,
+ *     mu_h   = exp(theta_mu_h) - exp(-theta_mu_h),
+ *
+ * with eps added for every theta_beta (bam_params.prior = BAM_PRIOR_THETA).
+ *
  * Conventions shared by every entry point
  *  - Tensors are dense, row-major, in device memory, 16-byte aligned:
  *    q, k, v, o, dO, dq, dk, dv are [B, H, T, D]; lse is [B, H, T].
@@ -54,9 +62,20 @@ typedef enum {
   BAM_ERR_WORKSPACE = 5    /* workspace missing, misaligned or too small      */
 } bam_status;
 
+/* Parameterisations of the prior (bam_params.prior). */
+enum {
+  BAM_PRIOR_ALPHA = 0, /* b = -(u/alpha)^beta; alpha > 0; eps clamps u when beta <= 0 */
+  BAM_PRIOR_THETA = 1  /* b = -exp(theta_alpha)(|d - mu| + eps)^theta_beta,
+                          mu = 2 sinh(theta_mu); any real thetas; eps always added */
+};
+
 /* Per-head prior and SSMax parameters.  alpha, beta, mu, s point to device
- * fp32 arrays of length H.  alpha_h > 0.  s is read only when ssmax != 0.
- * eps is the clamp of |d - mu| used when beta_h <= 0 (README: 1e-5). */
+ * fp32 arrays of length H; s is read only when ssmax != 0.  With
+ * BAM_PRIOR_ALPHA: alpha_h > 0, and eps (README: 1e-5) is the clamp of
+ * |d - mu| used when beta_h <= 0.  With BAM_PRIOR_THETA: alpha, beta, mu hold
+ * theta_alpha, theta_beta, theta_mu, eps is added to |d - mu| for every head,
+ * and bam_attn_bwd's dalpha, dbeta, dmu are the gradients with respect to
+ * those thetas.  eps > 0 in both. */
 typedef struct {
   const float* alpha;
   const float* beta;
@@ -65,6 +84,7 @@ typedef struct {
   float eps;
   int causal; /* 1: key j visible to query i iff j <= i; 0: all keys visible */
   int ssmax;  /* 1: Scalable-Softmax logit scale s_h * ln(n_i)               */
+  int prior;  /* BAM_PRIOR_ALPHA or BAM_PRIOR_THETA                         */
 } bam_params;
 
 enum { BAM_OP_FWD = 0, BAM_OP_BWD = 1, BAM_OP_DECODE = 2 };
@@ -86,7 +106,8 @@ bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, in
  * backward).  q, k, v, dO: bf16 [B,H,T,D]; o and lse: the forward's outputs
  * (o fp32 when o_fp32 != 0, else bf16).  Outputs: dq, dk, dv bf16
  * [B,H,T,D]; dalpha, dbeta, dmu, ds fp32 [H], overwritten, summed over the
- * batch (ds is written as 0 when ssmax == 0). */
+ * batch (ds is written as 0 when ssmax == 0); with BAM_PRIOR_THETA the first
+ * three are d/dtheta_alpha, d/dtheta_beta, d/dtheta_mu. */
 bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                         int o_fp32, const float* lse, const void* dO, void* dq, void* dk,
                         void* dv, float* dalpha, float* dbeta, float* dmu, float* ds, int B,

@@ -57,8 +57,8 @@ def test_workspace_sizes(lib):
 FAKE = 0x7F0000000000  # 256-aligned, never dereferenced: every call below fails first
 
 
-def _params(eps=1e-5, causal=1, ssmax=0, s=FAKE):
-    return ba.BamParams(FAKE, FAKE, FAKE, s, eps, causal, ssmax)
+def _params(eps=1e-5, causal=1, ssmax=0, s=FAKE, prior=ba.BAM_PRIOR_ALPHA):
+    return ba.BamParams(FAKE, FAKE, FAKE, s, eps, causal, ssmax, prior)
 
 
 def _fwd(lib, q=FAKE, o=FAKE, B=1, H=1, T=16, D=64, p=None, ws=FAKE, ws_bytes=1 << 30):
@@ -78,6 +78,8 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, p=_params(eps=0.0)) == ba.BAM_ERR_INVALID_ARG
     assert _fwd(lib, p=_params(ssmax=1, s=0)) == ba.BAM_ERR_INVALID_ARG
     assert _fwd(lib, p=_params(causal=2)) == ba.BAM_ERR_INVALID_ARG
+    assert _fwd(lib, p=_params(prior=2)) == ba.BAM_ERR_INVALID_ARG
+    assert _fwd(lib, p=_params(prior=-1)) == ba.BAM_ERR_INVALID_ARG
     assert _fwd(lib, ws=0) == ba.BAM_ERR_WORKSPACE
     assert _fwd(lib, ws=FAKE + 16) == ba.BAM_ERR_WORKSPACE         # not 256-aligned
     assert _fwd(lib, ws_bytes=100) == ba.BAM_ERR_WORKSPACE
@@ -116,3 +118,13 @@ def test_profile_events_bounds(lib):
 def test_check_status_rejects_bad_workspace(lib):
     assert lib.bam_attn_check_status(None, None) == ba.BAM_ERR_WORKSPACE
     assert lib.bam_attn_check_status(ctypes.c_void_p(FAKE + 8), None) == ba.BAM_ERR_WORKSPACE
+
+
+def test_prior_codes_and_params_layout_match_the_header():
+    text = open(HEADER).read()
+    assert int(re.search(r"BAM_PRIOR_ALPHA\s*=\s*(\d+)", text).group(1)) == ba.BAM_PRIOR_ALPHA
+    assert int(re.search(r"BAM_PRIOR_THETA\s*=\s*(\d+)", text).group(1)) == ba.BAM_PRIOR_THETA
+    body = re.search(r"typedef struct \{(.*?)\} bam_params;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"(\w+)\s*;", body)
+    assert fields == [f[0] for f in ba.BamParams._fields_]

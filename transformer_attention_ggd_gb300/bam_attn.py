@@ -27,6 +27,7 @@ BAM_ERR_TIMEOUT = 4
 BAM_ERR_WORKSPACE = 5
 
 BAM_OP_FWD, BAM_OP_BWD, BAM_OP_DECODE = 0, 1, 2
+BAM_PRIOR_ALPHA, BAM_PRIOR_THETA = 0, 1
 
 BAM_KERNEL_TABLE = 0
 BAM_KERNEL_FWD = 1
@@ -69,6 +70,7 @@ class BamParams(ctypes.Structure):
         ("eps", ctypes.c_float),
         ("causal", ctypes.c_int),
         ("ssmax", ctypes.c_int),
+        ("prior", ctypes.c_int),
     ]
 
 
@@ -124,11 +126,13 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def make_params(alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False) -> BamParams:
-    """alpha, beta, mu, s: float32 CUDA tensors of length H (kept alive by the caller)."""
+def make_params(alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False,
+                prior=BAM_PRIOR_ALPHA) -> BamParams:
+    """alpha, beta, mu, s: float32 CUDA tensors of length H (kept alive by the caller).
+    prior: BAM_PRIOR_ALPHA, or BAM_PRIOR_THETA when alpha, beta, mu hold the thetas."""
     return BamParams(alpha.data_ptr(), beta.data_ptr(), mu.data_ptr(),
                      s.data_ptr() if s is not None else None, float(eps), int(bool(causal)),
-                     int(bool(ssmax)))
+                     int(bool(ssmax)), int(prior))
 
 
 def _check(status: int, where: str):
@@ -216,35 +220,37 @@ def workspace(op: int, B: int, H: int, T: int, device="cuda"):
 
 
 def attention_forward(q, k, v, alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False,
-                      o_dtype=None, ws=None, stream=None):
-    """q, k, v: bf16 [B,H,T,64] CUDA tensors -> (o, lse)."""
+                      o_dtype=None, ws=None, stream=None, prior=BAM_PRIOR_ALPHA):
+    """q, k, v: bf16 [B,H,T,64] CUDA tensors -> (o, lse).  With
+    prior=BAM_PRIOR_THETA, alpha, beta, mu are theta_alpha, theta_beta, theta_mu."""
     import torch
     B, H, T, D = q.shape
     o = torch.empty((B, H, T, D), dtype=o_dtype or torch.float32, device=q.device)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     if ws is None:
         ws = workspace(BAM_OP_FWD, B, H, T, q.device)
-    prm = make_params(alpha, beta, mu, s, eps, causal, ssmax)
+    prm = make_params(alpha, beta, mu, s, eps, causal, ssmax, prior)
     bam_attn_fwd(q, k, v, o, lse, prm, ws, stream)
     return o, lse
 
 
 def attention_backward(q, k, v, o, lse, dO, alpha, beta, mu, s=None, eps=1e-5, causal=True,
-                       ssmax=False, ws=None, stream=None):
-    """Returns dq, dk, dv (bf16) and dalpha, dbeta, dmu, ds (fp32 [H])."""
+                       ssmax=False, ws=None, stream=None, prior=BAM_PRIOR_ALPHA):
+    """Returns dq, dk, dv (bf16) and dalpha, dbeta, dmu, ds (fp32 [H]); with
+    prior=BAM_PRIOR_THETA the three prior gradients are the thetas'."""
     import torch
     B, H, T, D = q.shape
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     g = [torch.empty(H, dtype=torch.float32, device=q.device) for _ in range(4)]
     if ws is None:
         ws = workspace(BAM_OP_BWD, B, H, T, q.device)
-    prm = make_params(alpha, beta, mu, s, eps, causal, ssmax)
+    prm = make_params(alpha, beta, mu, s, eps, causal, ssmax, prior)
     bam_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, g[0], g[1], g[2], g[3], prm, ws, stream)
     return dq, dk, dv, g[0], g[1], g[2], g[3]
 
 
 def attention_decode(q, kc, vc, alpha, beta, mu, s=None, eps=1e-5, ssmax=False, o_dtype=None,
-                     ws=None, stream=None):
+                     ws=None, stream=None, prior=BAM_PRIOR_ALPHA):
     """q: bf16 [B,H,64]; kc, vc: bf16 [B,H,Tkv,64] -> (o [B,H,64], lse [B,H])."""
     import torch
     B, H, Tkv, D = kc.shape
@@ -252,6 +258,6 @@ def attention_decode(q, kc, vc, alpha, beta, mu, s=None, eps=1e-5, ssmax=False, 
     lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
     if ws is None:
         ws = workspace(BAM_OP_DECODE, B, H, Tkv, q.device)
-    prm = make_params(alpha, beta, mu, s, eps, True, ssmax)
+    prm = make_params(alpha, beta, mu, s, eps, True, ssmax, prior)
     bam_attn_decode(q, kc, vc, o, lse, prm, ws, stream)
     return o, lse

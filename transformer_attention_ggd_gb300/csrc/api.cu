@@ -12,6 +12,8 @@
 #include "../../include/bam_attn.h"
 #include "bam_common.cuh"
 
+static_assert(BAM_PRIOR_THETA == bam::kPriorTheta, "prior codes of the ABI and the kernels");
+
 namespace bam {
 namespace {
 
@@ -118,6 +120,7 @@ bam_status check_params(const bam_params* p) {
   if (!(p->eps > 0.0f) || !std::isfinite(p->eps)) return BAM_ERR_INVALID_ARG;
   if ((p->causal != 0 && p->causal != 1) || (p->ssmax != 0 && p->ssmax != 1))
     return BAM_ERR_INVALID_ARG;
+  if (p->prior != BAM_PRIOR_ALPHA && p->prior != BAM_PRIOR_THETA) return BAM_ERR_INVALID_ARG;
   return BAM_OK;
 }
 
@@ -221,7 +224,7 @@ bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, in
   const TableGeom g = table_geom(T, p->causal);
 
   TableArgs ta{table, p->alpha, p->beta, p->mu, status, p->eps, H, g.len, g.off, 0,
-               kTableByDistance};
+               kTableByDistance, p->prior};
   cudaError_t e = launch_kernel(BAM_KERNEL_TABLE, stream, [&] { return launch_table(ta, stream); });
   if (e != cudaSuccess) return BAM_ERR_CUDA;
 
@@ -265,7 +268,7 @@ bam_status bam_attn_decode(const void* q, const void* kc, const void* vc, void* 
   float* table = reinterpret_cast<float*>(wsb + w.table);
 
   TableArgs ta{table, p->alpha, p->beta, p->mu, status, p->eps, H, w.tab_len, 0, Tkv,
-               kTableDecode};
+               kTableDecode, p->prior};
   cudaError_t e = launch_kernel(BAM_KERNEL_TABLE, stream, [&] { return launch_table(ta, stream); });
   if (e != cudaSuccess) return BAM_ERR_CUDA;
 
@@ -323,7 +326,7 @@ bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void*
 
   BwdArgs ba;
   ba.tab = TableArgs{table, p->alpha, p->beta, p->mu, status, p->eps, H, g.len, g.off, 0,
-                     kTableBackward};
+                     kTableBackward, p->prior};
   ba.o = o;
   ba.dO = static_cast<const uint16_t*>(dO);
   ba.lse = lse;

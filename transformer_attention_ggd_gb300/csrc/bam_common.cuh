@@ -15,6 +15,8 @@ namespace bam {
 constexpr int kHeadDim = 64;
 constexpr double kLog2e = 1.4426950408889634074;
 constexpr float kLn2f = 0.69314718055994530942f;
+// bam_params.prior value of the theta parameterisation (BAM_PRIOR_THETA).
+constexpr int kPriorTheta = 1;
 
 // Workspace: [0, 256) device status words, then op-specific regions, each
 // 256-byte aligned.
@@ -72,6 +74,7 @@ struct TableArgs {
   DevStatus* status;  // zeroed by block 0 (the first kernel of every call)
   float eps;
   int H, len, off, Tkv, mode;
+  int prior;  // BAM_PRIOR_ALPHA or BAM_PRIOR_THETA (alpha, beta, mu hold the thetas)
 };
 
 struct FwdArgs {

@@ -845,8 +845,9 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
   const volatile float* g = a.gacc;
   for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
     const float beta = a.beta[h], alpha = a.alpha[h];
-    // sum dS * b = ln(2) * sum dS * (b log2 e);  db/dalpha = -beta b / alpha
-    a.dalpha[h] = -(beta / alpha) * kLn2f * g[h];
+    // sum dS * b = ln(2) * sum dS * (b log2 e).  db/dalpha = -beta b / alpha;
+    // with the theta prior db/dtheta_alpha = b.
+    a.dalpha[h] = (a.tab.prior == kPriorTheta ? 1.0f : -(beta / alpha)) * kLn2f * g[h];
     a.dbeta[h] = g[a.H + h];
     a.dmu[h] = g[2 * a.H + h];
     a.ds[h] = a.ssmax ? g[3 * a.H + h] : 0.0f;

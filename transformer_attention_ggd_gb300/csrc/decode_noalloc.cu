@@ -76,6 +76,7 @@ extern "C" bam_status bam_attn_decode_noalloc(const void* q, const void* kc, con
   if (!p || !p->alpha || !p->beta || !p->mu || (p->ssmax && !p->s)) return BAM_ERR_INVALID_ARG;
   if (!(p->eps > 0.0f) || !(p->eps < 3.0e38f)) return BAM_ERR_INVALID_ARG;
   if (p->ssmax != 0 && p->ssmax != 1) return BAM_ERR_INVALID_ARG;
+  if (p->prior != BAM_PRIOR_ALPHA && p->prior != BAM_PRIOR_THETA) return BAM_ERR_INVALID_ARG;
   if (!q || !kc || !vc || !o) return BAM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(o) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3) != 0))
@@ -99,7 +100,7 @@ extern "C" bam_status bam_attn_decode_noalloc(const void* q, const void* kc, con
   float* table = reinterpret_cast<float*>(wsb + table_off);
 
   TableArgs ta{table, p->alpha, p->beta, p->mu, status, p->eps, H, tab_len, 0, Tkv,
-               kTableDecode};
+               kTableDecode, p->prior};
   cudaError_t e = launch_table(ta, stream);
   note_launches(1);
   if (e != cudaSuccess) return BAM_ERR_CUDA;

@@ -143,3 +143,17 @@ def random_params(H: int, rng: np.random.Generator, beta_lo=-1.0, beta_hi=2.0,
         else np.zeros(H, np.float32),
         "s": rng.uniform(0.3, 1.0, H).astype(np.float32),
     }
+
+
+def random_theta_params(H: int, rng: np.random.Generator) -> dict:
+    """Per-head thetas of the README parameterisation (values held in the
+    alpha, beta, mu slots): theta_alpha ~ U[-3, 1] (exp(theta_alpha) from
+    0.05 to 2.7, around the README's "slope" and "sampled" initialisations),
+    theta_beta ~ U[-1, 2] (both signs, and around its "linear" [0, 1] init),
+    theta_mu ~ U[-1, 1] (mu = 2 sinh(theta_mu) within +-2.4), s ~ U[0.3, 1]."""
+    return {
+        "alpha": rng.uniform(-3.0, 1.0, H).astype(np.float32),
+        "beta": rng.uniform(-1.0, 2.0, H).astype(np.float32),
+        "mu": rng.uniform(-1.0, 1.0, H).astype(np.float32),
+        "s": rng.uniform(0.3, 1.0, H).astype(np.float32),
+    }
