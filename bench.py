@@ -389,7 +389,8 @@ def run_ours(args, rank, world, dev, torch, dist):
 
 
 def extra_workloads(torch, dev, steps, peaks):
-    """Long-context prefill and decode (parity configurations), timed briefly."""
+    """Long-context prefill (causal, and the 32k one non-causal too) and decode
+    (parity configurations), timed briefly."""
     from transformer_attention_ggd_gb300 import bam_attn as ba
     from transformer_attention_ggd_gb300.inputs import make_inputs
 
@@ -398,12 +399,13 @@ def extra_workloads(torch, dev, steps, peaks):
     def bf(b):
         return torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
 
-    for cfg, reps in ((3, max(3, steps // 4)), (4, 2)):
+    for cfg, reps, causal in ((3, max(3, steps // 4), True), (4, 2, True),
+                              (3, max(3, steps // 4), False)):
         d = make_inputs(cfg)
         q, k, v = bf(d["q"]), bf(d["k"]), bf(d["v"])
         p = {n: torch.from_numpy(d[n]).to(dev) for n in ("alpha", "beta", "mu", "s")}
         B, H, T = d["B"], d["H"], d["T"]
-        prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, True, True)
+        prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, causal, True)
         o = torch.empty((B, H, T, D), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
         ws = ba.workspace(ba.BAM_OP_FWD, B, H, T, dev)
@@ -421,10 +423,10 @@ def extra_workloads(torch, dev, steps, peaks):
             ms.append(a.elapsed_time(b))
             kms.append(ka.elapsed_time(kb_))
         ba.bam_attn_profile_events(ba.BAM_KERNEL_FWD, None, None)
-        fl = pairs_causal(B, H, T) * 4 * D
+        fl = (pairs_causal(B, H, T) if causal else B * H * T * T) * 4 * D
         tf = fl / (statistics.median(ms) * 1e-3) / 1e12
         ktf = fl / (statistics.median(kms) * 1e-3) / 1e12
-        out[f"prefill_B{B}_H{H}_T{T}"] = {
+        out[f"prefill_{'' if causal else 'noncausal_'}B{B}_H{H}_T{T}"] = {
             "ms": round(statistics.median(ms), 4), "TFLOP/s": round(tf, 2),
             "fwd_kernel_TFLOP/s": round(ktf, 2),
             "frac_of_bf16_peak": round(ktf / peaks["bf16_tflops"], 4)}
@@ -459,6 +461,33 @@ def extra_workloads(torch, dev, steps, peaks):
     out[f"decode_B{B}_H{H}_Tkv{Tkv}"] = {
         "ms": round(statistics.median(ms), 4), "GB/s": round(gbs, 1),
         "decode_kernel_GB/s": round(kgbs, 1), "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4)}
+
+    # Ragged decode on the same cache: seeded lengths U[1, Tkv] per sequence;
+    # the bytes are those of the keys each sequence actually holds.
+    lens = np.random.default_rng(5005).integers(1, Tkv + 1, B)
+    lens[:3] = [1, Tkv, 64]
+    lens_d = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    ba.bam_attn_decode_varlen(q, kc, vc, lens_d, o, lse, prm, ws)
+    torch.cuda.synchronize()
+    ms, kms = [], []
+    for _ in range(max(5, steps // 2)):
+        ba.bam_attn_profile_events(ba.BAM_KERNEL_DECODE, ka, kb_)
+        a.record()
+        ba.bam_attn_decode_varlen(q, kc, vc, lens_d, o, lse, prm, ws)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+        kms.append(ka.elapsed_time(kb_))
+    ba.bam_attn_profile_events(ba.BAM_KERNEL_DECODE, None, None)
+    if ba.bam_attn_check_status(ws) != ba.BAM_OK:
+        raise RuntimeError("ragged decode status not clean")
+    kv_bytes = 2 * int(lens.sum()) * H * D * 2
+    gbs = kv_bytes / (statistics.median(ms) * 1e-3) / 1e9
+    kgbs = kv_bytes / (statistics.median(kms) * 1e-3) / 1e9
+    out[f"decode_varlen_B{B}_H{H}_Tmax{Tkv}"] = {
+        "ms": round(statistics.median(ms), 4), "mean_len": round(float(lens.mean()), 1),
+        "GB/s": round(gbs, 1), "decode_kernel_GB/s": round(kgbs, 1),
+        "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4)}
     return out
 
 

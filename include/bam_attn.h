@@ -123,9 +123,24 @@ bam_status bam_attn_decode(const void* q, const void* kc, const void* vc, void* 
                            float* lse, int B, int H, int Tkv, int D, const bam_params* p,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Ragged decode: as bam_attn_decode, but sequence b holds only
+ * cache_lens[b] keys, at positions 0 .. cache_lens[b]-1 of its [Tmax, D]
+ * cache rows (kc, vc: bf16 [B,H,Tmax,D]).  Its query sits at position
+ * cache_lens[b]-1, so key j is at distance cache_lens[b]-1-j, and
+ * n = cache_lens[b] for Scalable-Softmax.  cache_lens: device int32 [B],
+ * read on the device; each must lie in [1, Tmax].  A length outside it is
+ * clamped into it (no out-of-bounds access) and recorded, and
+ * bam_attn_check_status then returns BAM_ERR_INVALID_ARG.  The workspace is
+ * the one bam_attn_workspace_size(BAM_OP_DECODE, B, H, Tmax, D) gives. */
+bam_status bam_attn_decode_varlen(const void* q, const void* kc, const void* vc,
+                                  const int* cache_lens, void* o, int o_fp32, float* lse,
+                                  int B, int H, int Tmax, int D, const bam_params* p, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of
- * `ws`.  Returns BAM_OK, BAM_ERR_TIMEOUT (a device wait gave up) or
- * BAM_ERR_CUDA. */
+ * `ws`.  Returns BAM_OK, BAM_ERR_TIMEOUT (a device wait gave up),
+ * BAM_ERR_INVALID_ARG (a device-read argument was out of range: a ragged
+ * decode cache length) or BAM_ERR_CUDA. */
 bam_status bam_attn_check_status(void* ws, cudaStream_t stream);
 
 /* Static description of a status code. */

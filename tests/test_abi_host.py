@@ -109,6 +109,24 @@ def test_bwd_and_decode_argument_errors(lib):
                                16, None) == ba.BAM_ERR_WORKSPACE
 
 
+def test_decode_varlen_argument_errors(lib):
+    vp = ctypes.c_void_p
+    p = _params()
+    f = [vp(FAKE)] * 3
+    # missing or misaligned cache lengths
+    assert lib.bam_attn_decode_varlen(*f, None, vp(FAKE), 1, None, 2, 1, 16, 64, ctypes.byref(p),
+                                      vp(FAKE), 1 << 30, None) == ba.BAM_ERR_INVALID_ARG
+    assert lib.bam_attn_decode_varlen(*f, vp(FAKE + 2), vp(FAKE), 1, None, 2, 1, 16, 64,
+                                      ctypes.byref(p), vp(FAKE), 1 << 30,
+                                      None) == ba.BAM_ERR_INVALID_ARG
+    # Tmax invalid, workspace too small
+    assert lib.bam_attn_decode_varlen(*f, vp(FAKE), vp(FAKE), 1, None, 2, 1, 0, 64,
+                                      ctypes.byref(p), vp(FAKE), 1 << 30,
+                                      None) == ba.BAM_ERR_INVALID_ARG
+    assert lib.bam_attn_decode_varlen(*f, vp(FAKE), vp(FAKE), 1, None, 2, 1, 16, 64,
+                                      ctypes.byref(p), vp(FAKE), 16, None) == ba.BAM_ERR_WORKSPACE
+
+
 def test_profile_events_bounds(lib):
     assert lib.bam_attn_profile_events(-1, None, None) == ba.BAM_ERR_INVALID_ARG
     assert lib.bam_attn_profile_events(ba.BAM_KERNEL_COUNT, None, None) == ba.BAM_ERR_INVALID_ARG

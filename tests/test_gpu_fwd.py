@@ -147,6 +147,25 @@ def test_long_context_sampled_rows(cfg, per_head):
         np.testing.assert_allclose(lse[0, h, rows], lref, rtol=LSE_RTOL, atol=LSE_ATOL)
 
 
+def test_long_context_noncausal_sampled_rows():
+    """The 32k prefill with every key visible (the bench's non-causal line):
+    n = T for every row, distances of both signs."""
+    d = make_inputs(3)
+    o, lse = _run(d, d, False, True)
+    rng = np.random.default_rng(78)
+    B, H, T = d["B"], d["H"], d["T"]
+    for h in range(H):
+        rows = _sampled_rows(T, 12, rng)
+        sub = {x: d[x][0:1, h:h + 1] for x in "qkv"}
+        ph = {x: d[x][h:h + 1] for x in ("alpha", "beta", "mu", "s")}
+        oref, lref = oracle.fwd_rows(f64(sub["q"]), f64(sub["k"]), f64(sub["v"]), rows,
+                                     ph["alpha"], ph["beta"], ph["mu"], ph["s"], causal=False,
+                                     ssmax=True)
+        np.testing.assert_allclose(o[0, h, rows], oref, rtol=0, atol=O_ATOL,
+                                   err_msg=f"non-causal head {h}")
+        np.testing.assert_allclose(lse[0, h, rows], lref, rtol=LSE_RTOL, atol=LSE_ATOL)
+
+
 def test_repeat_calls_identical():
     rng = np.random.default_rng(3)
     bits = {n: normal_bits(rng, (2, 2, 700, 64)) for n in "qkv"}

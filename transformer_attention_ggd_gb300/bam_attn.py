@@ -44,6 +44,7 @@ EXPORTED = (
     "bam_attn_fwd",
     "bam_attn_bwd",
     "bam_attn_decode",
+    "bam_attn_decode_varlen",
     "bam_attn_check_status",
     "bam_status_string",
     "bam_attn_profile_events",
@@ -99,6 +100,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                      i, i, i, i, pp, vp, sz, vp]
         lib.bam_attn_decode.restype = i
         lib.bam_attn_decode.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp, sz, vp]
+        lib.bam_attn_decode_varlen.restype = i
+        lib.bam_attn_decode_varlen.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp, sz,
+                                               vp]
         lib.bam_attn_check_status.restype = i
         lib.bam_attn_check_status.argtypes = [vp, vp]
         lib.bam_status_string.restype = ctypes.c_char_p
@@ -181,6 +185,19 @@ def bam_attn_decode(q, kc, vc, o, lse, params: BamParams, ws, stream=None) -> No
     _check(st, "bam_attn_decode")
 
 
+def bam_attn_decode_varlen(q, kc, vc, cache_lens, o, lse, params: BamParams, ws,
+                           stream=None) -> None:
+    """cache_lens: int32 CUDA tensor [B] (each in [1, Tmax]); kc, vc: [B,H,Tmax,64]."""
+    import torch
+    B, H, Tmax, D = kc.shape
+    o_fp32 = 1 if o.dtype == torch.float32 else 0
+    st = load_library().bam_attn_decode_varlen(_ptr(q), _ptr(kc), _ptr(vc), _ptr(cache_lens),
+                                               _ptr(o), o_fp32, _ptr(lse), B, H, Tmax, D,
+                                               ctypes.byref(params), _ptr(ws), ws.numel(),
+                                               _stream(stream))
+    _check(st, "bam_attn_decode_varlen")
+
+
 def bam_attn_decode_noalloc(q, kc, vc, o, lse, params: BamParams, stream=None) -> None:
     """Decode for callers that cannot allocate device memory (plugin-style
     hosts that only pass input/output pointers; loops that cannot afford
@@ -260,4 +277,20 @@ def attention_decode(q, kc, vc, alpha, beta, mu, s=None, eps=1e-5, ssmax=False, 
         ws = workspace(BAM_OP_DECODE, B, H, Tkv, q.device)
     prm = make_params(alpha, beta, mu, s, eps, True, ssmax, prior)
     bam_attn_decode(q, kc, vc, o, lse, prm, ws, stream)
+    return o, lse
+
+
+def attention_decode_varlen(q, kc, vc, cache_lens, alpha, beta, mu, s=None, eps=1e-5,
+                            ssmax=False, o_dtype=None, ws=None, stream=None,
+                            prior=BAM_PRIOR_ALPHA):
+    """Ragged decode: q bf16 [B,H,64]; kc, vc bf16 [B,H,Tmax,64]; cache_lens
+    int32 [B] -> (o [B,H,64], lse [B,H])."""
+    import torch
+    B, H, Tmax, D = kc.shape
+    o = torch.empty((B, H, D), dtype=o_dtype or torch.float32, device=q.device)
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(BAM_OP_DECODE, B, H, Tmax, q.device)
+    prm = make_params(alpha, beta, mu, s, eps, True, ssmax, prior)
+    bam_attn_decode_varlen(q, kc, vc, cache_lens, o, lse, prm, ws, stream)
     return o, lse

@@ -183,6 +183,60 @@ namespace bam {
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 }  // namespace bam
 
+namespace bam {
+namespace {
+
+// bam_attn_decode and its ragged form (lens: device int32 [B], or null).
+bam_status decode_impl(const void* q, const void* kc, const void* vc, const int* lens, void* o,
+                       int o_fp32, float* lse, int B, int H, int Tkv, int D,
+                       const bam_params* p, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  bam_status s = check_sizes(B, H, Tkv, D);
+  if (s != BAM_OK) return s;
+  if ((s = check_params(p)) != BAM_OK) return s;
+  if (!q || !kc || !vc || !o) return BAM_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kc, 16) || !aligned(vc, 16) || !aligned(o, 16) ||
+      (lse && !aligned(lse, 4)))
+    return BAM_ERR_INVALID_ARG;
+  const DecWs w = dec_ws(B, H, Tkv);
+  if ((s = check_ws(ws, ws_bytes, w.total)) != BAM_OK) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  DevStatus* status = reinterpret_cast<DevStatus*>(wsb);
+  float* table = reinterpret_cast<float*>(wsb + w.table);
+
+  TableArgs ta{table, p->alpha, p->beta, p->mu, status, p->eps, H, w.tab_len, 0, Tkv,
+               kTableDecode, p->prior};
+  cudaError_t e = launch_kernel(BAM_KERNEL_TABLE, stream, [&] { return launch_table(ta, stream); });
+  if (e != cudaSuccess) return BAM_ERR_CUDA;
+
+  DecodeArgs da;
+  da.q = static_cast<const uint16_t*>(q);
+  da.kc = static_cast<const uint16_t*>(kc);
+  da.vc = static_cast<const uint16_t*>(vc);
+  da.lens = lens;
+  da.table = table;
+  da.s = p->s;
+  da.part = reinterpret_cast<float*>(wsb + w.part);
+  da.o = o;
+  da.lse = lse;
+  da.status = status;
+  da.B = B;
+  da.H = H;
+  da.Tkv = Tkv;
+  da.nsplit = w.nsplit;
+  da.chunk = w.chunk;
+  da.tab_len = w.tab_len;
+  da.ssmax = p->ssmax;
+  da.o_fp32 = o_fp32 ? 1 : 0;
+  e = launch_kernel(BAM_KERNEL_DECODE, stream, [&] { return launch_decode(da, stream); });
+  if (e != cudaSuccess) return BAM_ERR_CUDA;
+  e = launch_kernel(BAM_KERNEL_DECODE_COMBINE, stream,
+                    [&] { return launch_decode_combine(da, stream); });
+  return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace bam
+
 using namespace bam;
 
 extern "C" {
@@ -254,47 +308,16 @@ bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, in
 bam_status bam_attn_decode(const void* q, const void* kc, const void* vc, void* o, int o_fp32,
                            float* lse, int B, int H, int Tkv, int D, const bam_params* p,
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
-  bam_status s = check_sizes(B, H, Tkv, D);
-  if (s != BAM_OK) return s;
-  if ((s = check_params(p)) != BAM_OK) return s;
-  if (!q || !kc || !vc || !o) return BAM_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(kc, 16) || !aligned(vc, 16) || !aligned(o, 16) ||
-      (lse && !aligned(lse, 4)))
-    return BAM_ERR_INVALID_ARG;
-  const DecWs w = dec_ws(B, H, Tkv);
-  if ((s = check_ws(ws, ws_bytes, w.total)) != BAM_OK) return s;
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  DevStatus* status = reinterpret_cast<DevStatus*>(wsb);
-  float* table = reinterpret_cast<float*>(wsb + w.table);
+  return decode_impl(q, kc, vc, nullptr, o, o_fp32, lse, B, H, Tkv, D, p, ws, ws_bytes, stream);
+}
 
-  TableArgs ta{table, p->alpha, p->beta, p->mu, status, p->eps, H, w.tab_len, 0, Tkv,
-               kTableDecode, p->prior};
-  cudaError_t e = launch_kernel(BAM_KERNEL_TABLE, stream, [&] { return launch_table(ta, stream); });
-  if (e != cudaSuccess) return BAM_ERR_CUDA;
-
-  DecodeArgs da;
-  da.q = static_cast<const uint16_t*>(q);
-  da.kc = static_cast<const uint16_t*>(kc);
-  da.vc = static_cast<const uint16_t*>(vc);
-  da.table = table;
-  da.s = p->s;
-  da.part = reinterpret_cast<float*>(wsb + w.part);
-  da.o = o;
-  da.lse = lse;
-  da.status = status;
-  da.B = B;
-  da.H = H;
-  da.Tkv = Tkv;
-  da.nsplit = w.nsplit;
-  da.chunk = w.chunk;
-  da.tab_len = w.tab_len;
-  da.ssmax = p->ssmax;
-  da.o_fp32 = o_fp32 ? 1 : 0;
-  e = launch_kernel(BAM_KERNEL_DECODE, stream, [&] { return launch_decode(da, stream); });
-  if (e != cudaSuccess) return BAM_ERR_CUDA;
-  e = launch_kernel(BAM_KERNEL_DECODE_COMBINE, stream,
-                    [&] { return launch_decode_combine(da, stream); });
-  return cuda_status(e);
+bam_status bam_attn_decode_varlen(const void* q, const void* kc, const void* vc,
+                                  const int* cache_lens, void* o, int o_fp32, float* lse, int B,
+                                  int H, int Tmax, int D, const bam_params* p, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream) {
+  if (!cache_lens || !aligned(cache_lens, 4)) return BAM_ERR_INVALID_ARG;
+  return decode_impl(q, kc, vc, cache_lens, o, o_fp32, lse, B, H, Tmax, D, p, ws, ws_bytes,
+                     stream);
 }
 
 bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void* o, int o_fp32,
@@ -376,6 +399,7 @@ bam_status bam_attn_check_status(void* ws, cudaStream_t stream) {
   DevStatus st;
   if (cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return BAM_ERR_CUDA;
   if (cudaMemset(ws, 0, sizeof(st)) != cudaSuccess) return BAM_ERR_CUDA;
+  if (st.code == BAM_DEV_BAD_ARG && st.abort == 0) return BAM_ERR_INVALID_ARG;
   if (st.code != BAM_DEV_OK || st.abort != 0) return BAM_ERR_TIMEOUT;
   return BAM_OK;
 }

@@ -58,7 +58,9 @@ inline TableGeom table_geom(int T, int causal) {
 
 // Decode table: entry j of head h holds b_h(Tkv - 1 - j) * log2(e) for the
 // key at cache position j (0 beyond Tkv); rows padded to 64 entries.
-inline int decode_table_len(int Tkv) { return ((Tkv + 63) / 64) * 64; }
+// Entries of a decode table row: Tkv, plus room for the aligned 68-entry
+// stage window of the last stage (ragged decode starts windows at any entry).
+inline int decode_table_len(int Tkv) { return ((Tkv + 68 + 63) / 64) * 64; }
 
 enum TableMode : int {
   kTableByDistance = 0,  // forward: b only
@@ -92,6 +94,7 @@ struct DecodeArgs {
   const uint16_t* q;   // [BH, 64]
   const uint16_t* kc;  // [BH, Tkv, 64]
   const uint16_t* vc;
+  const int* lens;     // ragged decode: cache length of each sequence [B]; else null
   const float* table;  // [H, tab_len]
   const float* s;
   float* part;         // [BH, nsplit, 2 + 64]: m (log2 units), l, o[64]

@@ -97,7 +97,9 @@ struct DevStatus {
   int block;      // which block
 };
 
-enum : int { BAM_DEV_OK = 0, BAM_DEV_TIMEOUT = 1, BAM_DEV_ABORTED = 2 };
+// BAM_DEV_BAD_ARG: an argument only the device reads was out of range (a
+// cache length of the ragged decode); the kernel clamped it and went on.
+enum : int { BAM_DEV_OK = 0, BAM_DEV_TIMEOUT = 1, BAM_DEV_ABORTED = 2, BAM_DEV_BAD_ARG = 3 };
 
 // Wall-clock budget of one wait.  Normal waits last microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s

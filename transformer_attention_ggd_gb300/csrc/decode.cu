@@ -16,6 +16,13 @@
 // softmax in log2 units, p * v accumulated in registers.  The partial
 // (max, sum, unnormalised output) of each chunk goes to the workspace and a
 // second kernel merges the chunks of each (b, h).
+//
+// Ragged decode: sequence b holds len_b <= Tkv cached keys (the cache keeps
+// its [B, H, Tkv, 64] layout); its query sits at position len_b - 1 and
+// n = len_b.  Key j then reads table entry j + (Tkv - len_b) of the table
+// built for Tkv, so each stage copies an aligned 68-entry window and indexes
+// it with the remainder; chunks past len_b hold no keys and leave an empty
+// partial, which the merge skips.
 #include "bam_common.cuh"
 
 namespace bam {
@@ -23,6 +30,7 @@ namespace {
 
 constexpr int kDecStages = 4;
 constexpr int kDecKeys = 64;                 // keys per stage
+constexpr int kDecTab = kDecKeys + 4;        // table entries per stage (aligned window)
 constexpr int kDecConsumerWarps = 4;
 constexpr int kDecThreads = 32 * (kDecConsumerWarps + 1);
 constexpr int kStageBytes = kDecKeys * kHeadDim * 2;  // 8 KB of K (and of V)
@@ -32,7 +40,7 @@ constexpr int kPartStride = 2 + kHeadDim;   // m, l, o[64]
 struct __align__(128) DecSmem {
   uint8_t k[kDecStages][kStageBytes];
   uint8_t v[kDecStages][kStageBytes];
-  float tab[kDecStages][kDecKeys];
+  float tab[kDecStages][kDecTab];
   float red[kDecConsumerWarps][kPartStride];
   uint64_t full[kDecStages];
   uint64_t empty[kDecStages];
@@ -74,9 +82,19 @@ __global__ void __launch_bounds__(kDecThreads)
   const int sp = blockIdx.x;
   const int bh = blockIdx.y;
   const int h = bh % a.H;
+  // Keys of this (b, h): all Tkv, or the sequence's own cache length.
+  int len = a.Tkv;
+  bool bad_len = false;
+  if (a.lens) {
+    const int raw = __ldg(a.lens + bh / a.H);
+    len = min(max(raw, 1), a.Tkv);
+    bad_len = raw != len;
+  }
   const int kbeg = sp * a.chunk;
-  const int kend = min(a.Tkv, kbeg + a.chunk);
-  const int nst = (kend - kbeg + kDecKeys - 1) / kDecKeys;
+  const int kend = min(len, kbeg + a.chunk);
+  const int nst = kend > kbeg ? (kend - kbeg + kDecKeys - 1) / kDecKeys : 0;
+  const int tshift = a.Tkv - len;  // table entry of key j: j + tshift
+  const int trem = tshift & 3;     // offset of key 0 of a stage in its window
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -87,6 +105,8 @@ __global__ void __launch_bounds__(kDecThreads)
       mbar_init(&sm.empty[s], kDecConsumerWarps);
     }
     fence_barrier_init();
+    // Recorded after the wait: the table kernel clears the status word.
+    if (bad_len && sp == 0 && h == 0) atomicCAS(&a.status->code, BAM_DEV_OK, BAM_DEV_BAD_ARG);
   }
   __syncthreads();
 
@@ -106,11 +126,12 @@ __global__ void __launch_bounds__(kDecThreads)
         const int kb = kbeg + it * kDecKeys;
         const int nk = min(kDecKeys, kend - kb);
         const uint32_t bytes = static_cast<uint32_t>(nk) * kHeadDim * 2;
-        mbar_arrive_expect_tx(&sm.full[s], 2 * bytes + kDecKeys * 4);
+        mbar_arrive_expect_tx(&sm.full[s], 2 * bytes + kDecTab * 4);
         bulk_load(sm.k[s], a.kc + (row0 + kb) * kHeadDim, bytes, &sm.full[s]);
         bulk_load(sm.v[s], a.vc + (row0 + kb) * kHeadDim, bytes, &sm.full[s]);
-        bulk_load(sm.tab[s], a.table + static_cast<size_t>(h) * a.tab_len + kb, kDecKeys * 4,
-                  &sm.full[s]);
+        // 16-byte aligned window starting at or below entry kb + tshift
+        bulk_load(sm.tab[s], a.table + static_cast<size_t>(h) * a.tab_len + ((kb + tshift) & ~3),
+                  kDecTab * 4, &sm.full[s]);
         issued = it + 1;
       }
       for (int it = max(0, issued - kDecStages); it < issued; ++it)
@@ -122,7 +143,7 @@ __global__ void __launch_bounds__(kDecThreads)
     const int hf = lane & 1;                 // which 32 dimensions
     float cr;
     {
-      const float c = a.ssmax ? __ldg(a.s + h) * logf(static_cast<float>(a.Tkv)) * 0.125f
+      const float c = a.ssmax ? __ldg(a.s + h) * logf(static_cast<float>(len)) * 0.125f
                               : 0.125f;
       cr = c * 1.44269504088896341f;
     }
@@ -158,7 +179,7 @@ __global__ void __launch_bounds__(kDecThreads)
       }
       dot += __shfl_xor_sync(0xffffffffu, dot, 1);
       if (valid) {
-        const float z = dot + sm.tab[s][kk];
+        const float z = dot + sm.tab[s][kk + trem];
         if (z > m + kDecRescale) {
           const float corr = ex2_approx(m - z);
           l *= corr;

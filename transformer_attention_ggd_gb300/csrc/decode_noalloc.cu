@@ -109,6 +109,7 @@ extern "C" bam_status bam_attn_decode_noalloc(const void* q, const void* kc, con
   da.q = static_cast<const uint16_t*>(q);
   da.kc = static_cast<const uint16_t*>(kc);
   da.vc = static_cast<const uint16_t*>(vc);
+  da.lens = nullptr;
   da.table = table;
   da.s = p->s;
   da.part = reinterpret_cast<float*>(wsb + part_off);
