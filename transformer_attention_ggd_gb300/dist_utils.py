@@ -1,10 +1,15 @@
-"""Cross-rank helpers for data-parallel use of the attention path.
+"""Cross-rank helpers for sharded use of the attention path.
 
 The path shards by (b, h): forward, decode and dQ/dK/dV need no exchange.
-A data-parallel training step over a batch split across ranks has one real
-exchange, the sum of the per-head scalar gradients (dalpha, dbeta, dmu, ds:
-4*H floats), done here as one flat all-reduce.  Timing across ranks takes
-the slowest rank.
+Batch rows split across data-parallel ranks share the per-head prior and
+SSMax parameters, so a training step has one real exchange, the sum of the
+per-head scalar gradients (dalpha, dbeta, dmu, ds: 4*H floats of the heads
+the rank holds), done here as one flat all-reduce over the data-parallel
+group.  Heads split across tensor-parallel ranks (each rank holds the q, k, v
+columns of its heads, as a column-split QKV projection gives them) need no
+exchange at all: a head's scalar gradients come from that rank alone.  On a
+dp x tp mesh the reduction runs over the ranks that hold the same heads.
+Timing across ranks takes the slowest rank.
 """
 
 from __future__ import annotations
@@ -17,6 +22,49 @@ def shard_batch(B: int, rank: int, world: int) -> tuple[int, int]:
     base, extra = divmod(B, world)
     start = rank * base + min(rank, extra)
     return start, start + base + (1 if rank < extra else 0)
+
+
+def shard_heads(H: int, rank: int, world: int) -> tuple[int, int]:
+    """[start, stop) of the heads owned by tensor-parallel `rank`."""
+    return shard_batch(H, rank, world)
+
+
+def mesh_groups(dist, dp: int, tp: int):
+    """Process groups of a dp x tp mesh, rank = d * tp + t (every rank must
+    call this, in the same order).  Returns (dp_group, tp_group, d, t): the
+    ranks holding the same heads (t fixed) and the ranks holding the same
+    batch rows (d fixed)."""
+    world = dist.get_world_size()
+    if dp * tp != world:
+        raise ValueError(f"dp * tp = {dp * tp} != world size {world}")
+    rank = dist.get_rank()
+    d, t = divmod(rank, tp)
+    dp_group = tp_group = None
+    for tt in range(tp):
+        g = dist.new_group([dd * tp + tt for dd in range(dp)])
+        if tt == t:
+            dp_group = g
+    for dd in range(dp):
+        g = dist.new_group([dd * tp + tt for tt in range(tp)])
+        if dd == d:
+            tp_group = g
+    return dp_group, tp_group, d, t
+
+
+def sharded_attention_backward(q, k, v, o, lse, dO, alpha, beta, mu, s=None, *, dist=None,
+                               dp_group=None, backward=None, **kw):
+    """Backward of this rank's shard: q, k, v, o, lse, dO hold its batch rows
+    and heads, alpha, beta, mu, s its heads.  dq, dk, dv come back final; the
+    per-head scalar gradients are summed over `dp_group` (skipped when `dist`
+    is None or the group has one rank).  `backward` computes one shard; it
+    defaults to the library's ``attention_backward`` (keyword options such
+    as causal, ssmax, prior and eps pass through)."""
+    if backward is None:
+        from .bam_attn import attention_backward as backward
+    dq, dk, dv, *g = backward(q, k, v, o, lse, dO, alpha, beta, mu, s, **kw)
+    if dist is not None and dist.get_world_size(dp_group) > 1:
+        allreduce_head_grads(g, dist, dp_group)
+    return (dq, dk, dv, *g)
 
 
 def allreduce_head_grads(grads, dist, group=None):
