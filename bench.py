@@ -557,7 +557,8 @@ def run_reference(args):
     }
 
 
-PROFILE_CASES = ("train", "prefill32k", "prefill262k", "decode")
+PROFILE_CASES = ("train", "prefill32k", "prefill262k", "decode", "decode_varlen",
+                 "prefill32k_noncausal")
 
 
 def profile_case(name, warmup):
@@ -570,18 +571,28 @@ def profile_case(name, warmup):
 
     __graft_entry__.build()
     dev = torch.device("cuda", torch.cuda.current_device())
-    cfg = {"train": 2, "prefill32k": 3, "prefill262k": 4, "decode": 5}[name]
+    cfg = {"train": 2, "prefill32k": 3, "prefill262k": 4, "decode": 5, "decode_varlen": 5,
+           "prefill32k_noncausal": 3}[name]
+    causal = name != "prefill32k_noncausal"
     d = make_inputs(cfg)
 
     def bf(b):
         return torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
 
     p = {n: torch.from_numpy(d[n]).to(dev) for n in ("alpha", "beta", "mu", "s")}
-    prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, True, True)
+    prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, causal, True)
     B, H, T = d["B"], d["H"], d["T"]
     q, k, v = bf(d["q"]), bf(d["k"]), bf(d["v"])
     for _ in range(warmup + 1):
-        if name == "decode":
+        if name == "decode_varlen":
+            lens = np.random.default_rng(5005).integers(1, T + 1, B)
+            lens[:3] = [1, T, 64]
+            lens_d = torch.from_numpy(lens.astype(np.int32)).to(dev)
+            o = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+            ws = ba.workspace(ba.BAM_OP_DECODE, B, H, T, dev)
+            ba.bam_attn_decode_varlen(q, k, v, lens_d, o, lse, prm, ws)
+        elif name == "decode":
             o = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
             lse = torch.empty((B, H), dtype=torch.float32, device=dev)
             ws = ba.workspace(ba.BAM_OP_DECODE, B, H, T, dev)
