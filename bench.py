@@ -488,6 +488,42 @@ def extra_workloads(torch, dev, steps, peaks):
         "ms": round(statistics.median(ms), 4), "mean_len": round(float(lens.mean()), 1),
         "GB/s": round(gbs, 1), "decode_kernel_GB/s": round(kgbs, 1),
         "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4)}
+
+    # Paged decode: the same ragged cache in 256-key pages, randomly permuted
+    # (page p of the [B * Tkv/256] blocks stored at slot perm[p]).
+    page = 256
+    mb = Tkv // page
+    perm = torch.randperm(B * mb, generator=torch.Generator().manual_seed(6)).to(dev)
+    table = perm.view(B, mb).to(torch.int32)
+    pools = []
+    for c in (kc, vc):
+        blocks = c.view(B, H, mb, page, D).permute(0, 2, 1, 3, 4).reshape(B * mb, H, page, D)
+        pool = torch.empty_like(blocks)
+        pool[perm] = blocks
+        pools.append(pool)
+        del blocks
+    ba.bam_attn_decode_paged(q, pools[0], pools[1], table, lens_d, o, lse, prm, ws)
+    torch.cuda.synchronize()
+    ms, kms = [], []
+    for _ in range(max(5, steps // 2)):
+        ba.bam_attn_profile_events(ba.BAM_KERNEL_DECODE, ka, kb_)
+        a.record()
+        ba.bam_attn_decode_paged(q, pools[0], pools[1], table, lens_d, o, lse, prm, ws)
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+        kms.append(ka.elapsed_time(kb_))
+    ba.bam_attn_profile_events(ba.BAM_KERNEL_DECODE, None, None)
+    if ba.bam_attn_check_status(ws) != ba.BAM_OK:
+        raise RuntimeError("paged decode status not clean")
+    gbs = kv_bytes / (statistics.median(ms) * 1e-3) / 1e9
+    kgbs = kv_bytes / (statistics.median(kms) * 1e-3) / 1e9
+    out[f"decode_paged{page}_B{B}_H{H}_Tmax{Tkv}"] = {
+        "ms": round(statistics.median(ms), 4), "mean_len": round(float(lens.mean()), 1),
+        "GB/s": round(gbs, 1), "decode_kernel_GB/s": round(kgbs, 1),
+        "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4)}
+    del pools
+    torch.cuda.empty_cache()
     return out
 
 

@@ -137,10 +137,25 @@ bam_status bam_attn_decode_varlen(const void* q, const void* kc, const void* vc,
                                   int B, int H, int Tmax, int D, const bam_params* p, void* ws,
                                   size_t ws_bytes, cudaStream_t stream);
 
+/* Paged decode: as bam_attn_decode_varlen, with the cache in pages.
+ * k_pages, v_pages: bf16 [num_pages, H, page, D]; page is a multiple of 64.
+ * block_table: device int32 [B, max_blocks]; logical block i of sequence b
+ * (its keys i*page .. i*page+page-1) is page block_table[b*max_blocks + i].
+ * cache_lens: device int32 [B], each in [1, max_blocks*page]; only the blocks
+ * that hold a sequence's keys are read.  Out-of-range lengths or page numbers
+ * are clamped on the device (page 0) and reported by bam_attn_check_status as
+ * BAM_ERR_INVALID_ARG.  The workspace is the one
+ * bam_attn_workspace_size(BAM_OP_DECODE, B, H, max_blocks*page, D) gives. */
+bam_status bam_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                 const int* block_table, const int* cache_lens, void* o,
+                                 int o_fp32, float* lse, int B, int H, int page, int max_blocks,
+                                 int num_pages, int D, const bam_params* p, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of
  * `ws`.  Returns BAM_OK, BAM_ERR_TIMEOUT (a device wait gave up),
- * BAM_ERR_INVALID_ARG (a device-read argument was out of range: a ragged
- * decode cache length) or BAM_ERR_CUDA. */
+ * BAM_ERR_INVALID_ARG (a device-read argument was out of range: a ragged or
+ * paged decode's cache length or page number) or BAM_ERR_CUDA. */
 bam_status bam_attn_check_status(void* ws, cudaStream_t stream);
 
 /* Static description of a status code. */

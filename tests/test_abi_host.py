@@ -127,6 +127,25 @@ def test_decode_varlen_argument_errors(lib):
                                       ctypes.byref(p), vp(FAKE), 16, None) == ba.BAM_ERR_WORKSPACE
 
 
+def test_decode_paged_argument_errors(lib):
+    vp = ctypes.c_void_p
+    p = _params()
+    f = [vp(FAKE)] * 3
+
+    def call(bt=FAKE, lens=FAKE, page=64, max_blocks=4, num_pages=8, ws_bytes=1 << 30):
+        return lib.bam_attn_decode_paged(*f, vp(bt), vp(lens), vp(FAKE), 1, None, 2, 1, page,
+                                         max_blocks, num_pages, 64, ctypes.byref(p), vp(FAKE),
+                                         ws_bytes, None)
+    assert call(bt=0) == ba.BAM_ERR_INVALID_ARG
+    assert call(lens=0) == ba.BAM_ERR_INVALID_ARG
+    assert call(bt=FAKE + 2) == ba.BAM_ERR_INVALID_ARG
+    assert call(page=32) == ba.BAM_ERR_INVALID_ARG
+    assert call(page=96) == ba.BAM_ERR_INVALID_ARG
+    assert call(max_blocks=0) == ba.BAM_ERR_INVALID_ARG
+    assert call(num_pages=0) == ba.BAM_ERR_INVALID_ARG
+    assert call(ws_bytes=16) == ba.BAM_ERR_WORKSPACE
+
+
 def test_profile_events_bounds(lib):
     assert lib.bam_attn_profile_events(-1, None, None) == ba.BAM_ERR_INVALID_ARG
     assert lib.bam_attn_profile_events(ba.BAM_KERNEL_COUNT, None, None) == ba.BAM_ERR_INVALID_ARG

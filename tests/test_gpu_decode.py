@@ -156,3 +156,89 @@ def test_varlen_full_size():
     oref, lref = _varlen_ref(d["q"], d["k"], d["v"], lens, d, True)
     np.testing.assert_allclose(o, oref, rtol=0, atol=O_ATOL)
     np.testing.assert_allclose(lse, lref, rtol=LSE_RTOL, atol=LSE_ATOL)
+
+
+# ---------------------------------------------------------------- paged decode
+
+def _to_pages(kc, lens, page, rng, extra_pages=3, junk=True):
+    """Scatter a contiguous [B,H,Tmax,64] cache into randomly permuted pages
+    [num_pages,H,page,64] (unused pages and the tails of partly used ones hold
+    junk, or zeros); block-table entries past a sequence's length are -1
+    (never read)."""
+    B, H, Tmax, D = kc.shape
+    max_blocks = Tmax // page
+    used = [(b, i) for b in range(B) for i in range((lens[b] + page - 1) // page)]
+    num_pages = len(used) + extra_pages
+    perm = rng.permutation(num_pages)[:len(used)]
+    shape = (num_pages, H, page, D)
+    pages = rng.integers(0, 1 << 16, shape).astype(np.uint16) if junk else np.zeros(shape,
+                                                                                      np.uint16)
+    table = np.full((B, max_blocks), -1, np.int32)
+    for (b, i), pg in zip(used, perm):
+        table[b, i] = pg
+        pages[pg] = kc[b, :, i * page:(i + 1) * page]
+    return pages, table
+
+
+def _paged(q, kp, vp, table, lens, prm, ssmax):
+    t = params_dev(prm)
+    B, H = q.shape[:2]
+    ws = ba.workspace(ba.BAM_OP_DECODE, B, H, kp.shape[2] * table.shape[1])
+    o, lse = ba.attention_decode_paged(
+        dev_bf16(q), dev_bf16(kp), dev_bf16(vp), torch.from_numpy(table).cuda(),
+        torch.from_numpy(np.asarray(lens, np.int32)).cuda(), t["alpha"], t["beta"], t["mu"],
+        t["s"], ssmax=ssmax, ws=ws)
+    status = ba.bam_attn_check_status(ws)
+    return o.float().cpu().numpy(), lse.cpu().numpy(), status
+
+
+@pytest.mark.parametrize("page", [64, 256])
+def test_paged_equals_contiguous_ragged(page):
+    """Same kernels, same order of arithmetic: only the source addresses of the
+    K/V stages differ, so the results are bit-identical."""
+    rng = np.random.default_rng(70 + page)
+    B, H, Tmax = 6, 3, 1024
+    lens = [1, 63, 64, 65, 700, 1024]
+    q = normal_bits(rng, (B, H, 64))
+    kc, vc = normal_bits(rng, (B, H, Tmax, 64)), normal_bits(rng, (B, H, Tmax, 64))
+    prm = random_params(H, rng, mu_hi=5.0)
+    kp, table = _to_pages(kc, lens, page, np.random.default_rng(1))
+    vp, _ = _to_pages(vc, lens, page, np.random.default_rng(1))
+    o1, l1, st1 = _paged(q, kp, vp, table, lens, prm, True)
+    o2, l2, st2 = _varlen(q, kc, vc, lens, prm, True)
+    assert st1 == ba.BAM_OK and st2 == ba.BAM_OK
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    oref, lref = _varlen_ref(q, kc, vc, lens, prm, True)
+    np.testing.assert_allclose(o1, oref, rtol=0, atol=O_ATOL)
+
+
+def test_paged_bad_page_is_reported():
+    rng = np.random.default_rng(72)
+    B, H, Tmax, page = 2, 2, 256, 64
+    lens = [200, 256]
+    q = normal_bits(rng, (B, H, 64))
+    kc, vc = normal_bits(rng, (B, H, Tmax, 64)), normal_bits(rng, (B, H, Tmax, 64))
+    prm = random_params(H, rng)
+    kp, table = _to_pages(kc, lens, page, np.random.default_rng(2))
+    vp, _ = _to_pages(vc, lens, page, np.random.default_rng(2))
+    table[1, 2] = kp.shape[0] + 5   # a used block pointing past the pool
+    o, lse, st = _paged(q, kp, vp, table, lens, prm, True)
+    assert st == ba.BAM_ERR_INVALID_ARG
+    assert np.all(np.isfinite(o))
+
+
+def test_paged_full_size():
+    """B=64 H=12 with lengths U[1, 32768] in 256-key pages, permuted: equal to
+    the contiguous ragged decode (the bench's paged line)."""
+    d = make_inputs(5)
+    B, H, Tmax = d["B"], d["H"], d["T"]
+    lens = np.random.default_rng(5005).integers(1, Tmax + 1, B)
+    lens[:3] = [1, Tmax, 64]
+    kp, table = _to_pages(d["k"], lens, 256, np.random.default_rng(6), extra_pages=0, junk=False)
+    vp, _ = _to_pages(d["v"], lens, 256, np.random.default_rng(6), extra_pages=0, junk=False)
+    o1, l1, st1 = _paged(d["q"], kp, vp, table, lens, d, True)
+    o2, l2, st2 = _varlen(d["q"], d["k"], d["v"], lens, d, True)
+    assert st1 == ba.BAM_OK and st2 == ba.BAM_OK
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)

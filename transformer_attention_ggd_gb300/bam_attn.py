@@ -45,6 +45,7 @@ EXPORTED = (
     "bam_attn_bwd",
     "bam_attn_decode",
     "bam_attn_decode_varlen",
+    "bam_attn_decode_paged",
     "bam_attn_check_status",
     "bam_status_string",
     "bam_attn_profile_events",
@@ -100,6 +101,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                      i, i, i, i, pp, vp, sz, vp]
         lib.bam_attn_decode.restype = i
         lib.bam_attn_decode.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp, sz, vp]
+        lib.bam_attn_decode_paged.restype = i
+        lib.bam_attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, pp,
+                                              vp, sz, vp]
         lib.bam_attn_decode_varlen.restype = i
         lib.bam_attn_decode_varlen.argtypes = [vp, vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp, sz,
                                                vp]
@@ -198,6 +202,22 @@ def bam_attn_decode_varlen(q, kc, vc, cache_lens, o, lse, params: BamParams, ws,
     _check(st, "bam_attn_decode_varlen")
 
 
+def bam_attn_decode_paged(q, k_pages, v_pages, block_table, cache_lens, o, lse,
+                          params: BamParams, ws, stream=None) -> None:
+    """k_pages, v_pages: [num_pages, H, page, 64]; block_table int32 [B, max_blocks];
+    cache_lens int32 [B]."""
+    import torch
+    num_pages, H, page, D = k_pages.shape
+    B, max_blocks = block_table.shape
+    o_fp32 = 1 if o.dtype == torch.float32 else 0
+    st = load_library().bam_attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                              _ptr(block_table), _ptr(cache_lens), _ptr(o),
+                                              o_fp32, _ptr(lse), B, H, page, max_blocks,
+                                              num_pages, D, ctypes.byref(params), _ptr(ws),
+                                              ws.numel(), _stream(stream))
+    _check(st, "bam_attn_decode_paged")
+
+
 def bam_attn_decode_noalloc(q, kc, vc, o, lse, params: BamParams, stream=None) -> None:
     """Decode for callers that cannot allocate device memory (plugin-style
     hosts that only pass input/output pointers; loops that cannot afford
@@ -293,4 +313,21 @@ def attention_decode_varlen(q, kc, vc, cache_lens, alpha, beta, mu, s=None, eps=
         ws = workspace(BAM_OP_DECODE, B, H, Tmax, q.device)
     prm = make_params(alpha, beta, mu, s, eps, True, ssmax, prior)
     bam_attn_decode_varlen(q, kc, vc, cache_lens, o, lse, prm, ws, stream)
+    return o, lse
+
+
+def attention_decode_paged(q, k_pages, v_pages, block_table, cache_lens, alpha, beta, mu,
+                           s=None, eps=1e-5, ssmax=False, o_dtype=None, ws=None, stream=None,
+                           prior=BAM_PRIOR_ALPHA):
+    """Paged decode: q bf16 [B,H,64]; k_pages, v_pages bf16 [num_pages,H,page,64];
+    block_table int32 [B, max_blocks]; cache_lens int32 [B] -> (o, lse)."""
+    import torch
+    B, H, D = q.shape
+    page, max_blocks = k_pages.shape[2], block_table.shape[1]
+    o = torch.empty((B, H, D), dtype=o_dtype or torch.float32, device=q.device)
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(BAM_OP_DECODE, B, H, page * max_blocks, q.device)
+    prm = make_params(alpha, beta, mu, s, eps, True, ssmax, prior)
+    bam_attn_decode_paged(q, k_pages, v_pages, block_table, cache_lens, o, lse, prm, ws, stream)
     return o, lse

@@ -187,9 +187,17 @@ namespace bam {
 namespace {
 
 // bam_attn_decode and its ragged form (lens: device int32 [B], or null).
+// Paged form: block_table non-null, kc/vc [num_pages, H, page, D], Tkv the
+// longest sequence a block-table row can hold (max_blocks * page).
+struct Paging {
+  const int* block_table = nullptr;
+  int page = 0, max_blocks = 0, num_pages = 0;
+};
+
 bam_status decode_impl(const void* q, const void* kc, const void* vc, const int* lens, void* o,
                        int o_fp32, float* lse, int B, int H, int Tkv, int D,
-                       const bam_params* p, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                       const bam_params* p, void* ws, size_t ws_bytes, cudaStream_t stream,
+                       const Paging& pg = Paging()) {
   bam_status s = check_sizes(B, H, Tkv, D);
   if (s != BAM_OK) return s;
   if ((s = check_params(p)) != BAM_OK) return s;
@@ -213,6 +221,10 @@ bam_status decode_impl(const void* q, const void* kc, const void* vc, const int*
   da.kc = static_cast<const uint16_t*>(kc);
   da.vc = static_cast<const uint16_t*>(vc);
   da.lens = lens;
+  da.block_table = pg.block_table;
+  da.page = pg.page;
+  da.max_blocks = pg.max_blocks;
+  da.num_pages = pg.num_pages;
   da.table = table;
   da.s = p->s;
   da.part = reinterpret_cast<float*>(wsb + w.part);
@@ -309,6 +321,25 @@ bam_status bam_attn_decode(const void* q, const void* kc, const void* vc, void* 
                            float* lse, int B, int H, int Tkv, int D, const bam_params* p,
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
   return decode_impl(q, kc, vc, nullptr, o, o_fp32, lse, B, H, Tkv, D, p, ws, ws_bytes, stream);
+}
+
+bam_status bam_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                                 const int* block_table, const int* cache_lens, void* o,
+                                 int o_fp32, float* lse, int B, int H, int page, int max_blocks,
+                                 int num_pages, int D, const bam_params* p, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  if (!block_table || !aligned(block_table, 4) || !cache_lens || !aligned(cache_lens, 4))
+    return BAM_ERR_INVALID_ARG;
+  if (page < 64 || page % 64 != 0 || max_blocks < 1 || num_pages < 1) return BAM_ERR_INVALID_ARG;
+  const int64_t tmax = static_cast<int64_t>(page) * max_blocks;
+  if (tmax > (1 << 28)) return BAM_ERR_UNSUPPORTED;
+  Paging pg;
+  pg.block_table = block_table;
+  pg.page = page;
+  pg.max_blocks = max_blocks;
+  pg.num_pages = num_pages;
+  return decode_impl(q, k_pages, v_pages, cache_lens, o, o_fp32, lse, B, H,
+                     static_cast<int>(tmax), D, p, ws, ws_bytes, stream, pg);
 }
 
 bam_status bam_attn_decode_varlen(const void* q, const void* kc, const void* vc,

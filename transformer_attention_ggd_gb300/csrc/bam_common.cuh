@@ -95,6 +95,10 @@ struct DecodeArgs {
   const uint16_t* kc;  // [BH, Tkv, 64]
   const uint16_t* vc;
   const int* lens;     // ragged decode: cache length of each sequence [B]; else null
+  // Paged cache (block_table non-null): kc, vc are [num_pages, H, page, 64]
+  // and logical block i of sequence b is page block_table[b * max_blocks + i].
+  const int* block_table;
+  int page, max_blocks, num_pages;
   const float* table;  // [H, tab_len]
   const float* s;
   float* part;         // [BH, nsplit, 2 + 64]: m (log2 units), l, o[64]

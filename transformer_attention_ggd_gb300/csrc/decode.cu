@@ -23,6 +23,11 @@
 // built for Tkv, so each stage copies an aligned 68-entry window and indexes
 // it with the remainder; chunks past len_b hold no keys and leave an empty
 // partial, which the merge skips.
+//
+// Paged cache: K and V live in pages of `page` keys (a multiple of 64), laid
+// out [num_pages, H, page, 64]; a sequence's logical block i is the page its
+// block-table row names, so a 64-key stage is one contiguous run of a page
+// and only the producer's source address changes.
 #include "bam_common.cuh"
 
 namespace bam {
@@ -115,6 +120,7 @@ __global__ void __launch_bounds__(kDecThreads)
     if (lane == 0) {
       bool ok = (*ab == 0);
       int issued = 0;
+      bool bad_page = false;
       const size_t row0 = static_cast<size_t>(bh) * a.Tkv;
       for (int it = 0; ok && it < nst; ++it) {
         const int s = it % kDecStages;
@@ -127,8 +133,18 @@ __global__ void __launch_bounds__(kDecThreads)
         const int nk = min(kDecKeys, kend - kb);
         const uint32_t bytes = static_cast<uint32_t>(nk) * kHeadDim * 2;
         mbar_arrive_expect_tx(&sm.full[s], 2 * bytes + kDecTab * 4);
-        bulk_load(sm.k[s], a.kc + (row0 + kb) * kHeadDim, bytes, &sm.full[s]);
-        bulk_load(sm.v[s], a.vc + (row0 + kb) * kHeadDim, bytes, &sm.full[s]);
+        size_t key0 = row0 + kb;  // first key of the stage, in keys of the cache
+        if (a.block_table) {
+          int pg = __ldg(a.block_table + static_cast<size_t>(bh / a.H) * a.max_blocks +
+                         kb / a.page);
+          if (pg < 0 || pg >= a.num_pages) {
+            bad_page = true;
+            pg = 0;
+          }
+          key0 = (static_cast<size_t>(pg) * a.H + h) * a.page + kb % a.page;
+        }
+        bulk_load(sm.k[s], a.kc + key0 * kHeadDim, bytes, &sm.full[s]);
+        bulk_load(sm.v[s], a.vc + key0 * kHeadDim, bytes, &sm.full[s]);
         // 16-byte aligned window starting at or below entry kb + tshift
         bulk_load(sm.tab[s], a.table + static_cast<size_t>(h) * a.tab_len + ((kb + tshift) & ~3),
                   kDecTab * 4, &sm.full[s]);
@@ -136,6 +152,7 @@ __global__ void __launch_bounds__(kDecThreads)
       }
       for (int it = max(0, issued - kDecStages); it < issued; ++it)
         mbar_drain(&sm.full[it % kDecStages], (it / kDecStages) & 1);
+      if (bad_page) atomicCAS(&a.status->code, BAM_DEV_OK, BAM_DEV_BAD_ARG);
     }
   } else {
     // ------------------------------------------------------------ consumers

@@ -110,6 +110,8 @@ extern "C" bam_status bam_attn_decode_noalloc(const void* q, const void* kc, con
   da.kc = static_cast<const uint16_t*>(kc);
   da.vc = static_cast<const uint16_t*>(vc);
   da.lens = nullptr;
+  da.block_table = nullptr;
+  da.page = da.max_blocks = da.num_pages = 0;
   da.table = table;
   da.s = p->s;
   da.part = reinterpret_cast<float*>(wsb + part_off);
