@@ -594,7 +594,7 @@ def run_reference(args):
 
 
 PROFILE_CASES = ("train", "prefill32k", "prefill262k", "decode", "decode_varlen",
-                 "prefill32k_noncausal")
+                 "decode_paged", "prefill32k_noncausal")
 
 
 def profile_case(name, warmup):
@@ -608,7 +608,7 @@ def profile_case(name, warmup):
     __graft_entry__.build()
     dev = torch.device("cuda", torch.cuda.current_device())
     cfg = {"train": 2, "prefill32k": 3, "prefill262k": 4, "decode": 5, "decode_varlen": 5,
-           "prefill32k_noncausal": 3}[name]
+           "decode_paged": 5, "prefill32k_noncausal": 3}[name]
     causal = name != "prefill32k_noncausal"
     d = make_inputs(cfg)
 
@@ -620,14 +620,28 @@ def profile_case(name, warmup):
     B, H, T = d["B"], d["H"], d["T"]
     q, k, v = bf(d["q"]), bf(d["k"]), bf(d["v"])
     for _ in range(warmup + 1):
-        if name == "decode_varlen":
+        if name in ("decode_varlen", "decode_paged"):
             lens = np.random.default_rng(5005).integers(1, T + 1, B)
             lens[:3] = [1, T, 64]
             lens_d = torch.from_numpy(lens.astype(np.int32)).to(dev)
             o = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
             lse = torch.empty((B, H), dtype=torch.float32, device=dev)
             ws = ba.workspace(ba.BAM_OP_DECODE, B, H, T, dev)
-            ba.bam_attn_decode_varlen(q, k, v, lens_d, o, lse, prm, ws)
+            if name == "decode_varlen":
+                ba.bam_attn_decode_varlen(q, k, v, lens_d, o, lse, prm, ws)
+            else:
+                # the bench's layout: 256-key pages of every block, permuted
+                page, mb = 256, T // 256
+                perm = torch.randperm(B * mb, generator=torch.Generator().manual_seed(6)).to(dev)
+                pools = []
+                for c in (k, v):
+                    blk = c.view(B, H, mb, page, D).permute(0, 2, 1, 3, 4).reshape(B * mb, H,
+                                                                                  page, D)
+                    pool = torch.empty_like(blk)
+                    pool[perm] = blk
+                    pools.append(pool)
+                ba.bam_attn_decode_paged(q, pools[0], pools[1], perm.view(B, mb).to(torch.int32),
+                                         lens_d, o, lse, prm, ws)
         elif name == "decode":
             o = torch.empty((B, H, D), dtype=torch.bfloat16, device=dev)
             lse = torch.empty((B, H), dtype=torch.float32, device=dev)
