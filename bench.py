@@ -270,11 +270,12 @@ def run_ours(args, rank, world, dev, torch, dist):
     host_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
     nb = 2
     dev_in = [{n: torch.empty_like(t[n]) for n in host_in} for _ in range(nb)]
+    # The four per-head scalar gradients share one [4, H] buffer: one copy.
     dev_out = [([torch.empty_like(dq) for _ in range(3)],
-                [torch.empty(H, dtype=torch.float32, device=dev) for _ in range(4)])
+                torch.empty((4, H), dtype=torch.float32, device=dev))
                for _ in range(nb)]
     host_out = [[torch.empty_like(x, device="cpu").pin_memory() for x in (dq, dk, dv)]
-                + [torch.empty(H, dtype=torch.float32).pin_memory() for _ in range(4)]
+                + [torch.empty((4, H), dtype=torch.float32).pin_memory()]
                 for _ in range(nb)]
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for x in host_out[0])
@@ -321,7 +322,7 @@ def run_ours(args, rank, world, dev, torch, dist):
             if 2 <= i <= K + 1:  # D2H of step i-2
                 b = (i - 2) % nb
                 (gq, gk, gv), gs = dev_out[b]
-                pairs = list(zip(host_out[b], [gq, gk, gv] + gs))
+                pairs = list(zip(host_out[b], [gq, gk, gv, gs]))
                 for k_, (st, ev) in enumerate(((s_d2h, ev_out), (s_d2h2, ev_out2))):
                     with torch.cuda.stream(st):
                         st.wait_event(ev_cmp[b])
