@@ -70,12 +70,28 @@ def load_peaks():
             "source": "fallback"}
 
 
-def kernel_source_hash():
+# The files each profiled kernel is compiled from: its .cu, the headers it
+# includes, and the build script (compiler flags).
+KERNEL_SOURCES = {
+    "bam_bwd_kernel": ("bwd.cu", "table_eval.cuh", "bam_common.cuh", "bam_ptx.cuh"),
+    "bam_fwd_kernel": ("fwd.cu", "bam_common.cuh", "bam_ptx.cuh"),
+    "bam_decode_kernel": ("decode.cu", "bam_common.cuh", "bam_ptx.cuh"),
+}
+
+
+def kernel_source_hash(kernel=None):
+    """16 hex digits of sha256 over the sources of `kernel` (every file under
+    csrc/ when None)."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "transformer_attention_ggd_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    pkg = os.path.join(ROOT, "transformer_attention_ggd_gb300")
+    csrc = os.path.join(pkg, "csrc")
+    names = sorted(os.listdir(csrc)) if kernel is None else KERNEL_SOURCES[kernel]
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
+            h.update(f.read())
+    if kernel is not None:
+        with open(os.path.join(pkg, "build.py"), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -89,7 +105,7 @@ def profiled_traffic(kernel: str):
     with open(path) as f:
         t = json.load(f)
     entry = t.get(kernel)
-    if not entry or entry.get("source_hash") != kernel_source_hash():
+    if not entry or entry.get("source_hash") != kernel_source_hash(kernel.split("@")[0]):
         return None
     return entry.get("dram_bytes_per_launch")
 
