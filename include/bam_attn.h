@@ -158,6 +158,14 @@ bam_status bam_attn_decode_paged(const void* q, const void* k_pages, const void*
  * paged decode's cache length or page number) or BAM_ERR_CUDA. */
 bam_status bam_attn_check_status(void* ws, cudaStream_t stream);
 
+/* Self-test of the failure detection: launches one thread that waits, with
+ * the library's bounded wait, on a barrier nothing arrives at.  After the
+ * wait limit (2 s) it records BAM_ERR_TIMEOUT in the status word of `ws`
+ * (at least 256 bytes, 256-byte aligned) and returns; the context stays
+ * usable.  Read the result with bam_attn_check_status.  Not part of any
+ * attention call. */
+bam_status bam_attn_selftest_wait(void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* bam_status_string(bam_status s);
 

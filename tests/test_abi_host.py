@@ -146,6 +146,13 @@ def test_decode_paged_argument_errors(lib):
     assert call(ws_bytes=16) == ba.BAM_ERR_WORKSPACE
 
 
+def test_selftest_rejects_bad_workspace(lib):
+    vp = ctypes.c_void_p
+    assert lib.bam_attn_selftest_wait(None, 1 << 20, None) == ba.BAM_ERR_WORKSPACE
+    assert lib.bam_attn_selftest_wait(vp(FAKE + 16), 1 << 20, None) == ba.BAM_ERR_WORKSPACE
+    assert lib.bam_attn_selftest_wait(vp(FAKE), 128, None) == ba.BAM_ERR_WORKSPACE
+
+
 def test_profile_events_bounds(lib):
     assert lib.bam_attn_profile_events(-1, None, None) == ba.BAM_ERR_INVALID_ARG
     assert lib.bam_attn_profile_events(ba.BAM_KERNEL_COUNT, None, None) == ba.BAM_ERR_INVALID_ARG

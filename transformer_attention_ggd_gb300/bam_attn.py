@@ -51,6 +51,7 @@ EXPORTED = (
     "bam_attn_profile_events",
     "bam_attn_launch_count",
     "bam_attn_decode_noalloc",
+    "bam_attn_selftest_wait",
 )
 
 # Size of the fixed device scratch of bam_attn_decode_noalloc.
@@ -117,6 +118,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bam_attn_launch_count.argtypes = []
         lib.bam_attn_decode_noalloc.restype = i
         lib.bam_attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp]
+        lib.bam_attn_selftest_wait.restype = i
+        lib.bam_attn_selftest_wait.argtypes = [vp, sz, vp]
         _lib = lib
         return lib
 
@@ -230,6 +233,13 @@ def bam_attn_decode_noalloc(q, kc, vc, o, lse, params: BamParams, stream=None) -
                                                 _ptr(lse), B, H, Tkv, D, ctypes.byref(params),
                                                 _stream(stream))
     _check(st, "bam_attn_decode_noalloc")
+
+
+def bam_attn_selftest_wait(ws, stream=None) -> None:
+    """Launch the failure-detection self-test: a bounded wait that runs out
+    and records BAM_ERR_TIMEOUT in the status word of `ws` (about 2 s)."""
+    _check(load_library().bam_attn_selftest_wait(_ptr(ws), ws.numel(), _stream(stream)),
+           "bam_attn_selftest_wait")
 
 
 def bam_attn_check_status(ws, stream=None) -> int:

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libbam_attn.so")
-SOURCES = ["api.cu", "table.cu", "fwd.cu", "bwd.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "table.cu", "fwd.cu", "bwd.cu", "decode.cu", "decode_noalloc.cu",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          f"-I{os.path.join(ROOT, 'include')}"]
