@@ -110,6 +110,18 @@ def profiled_traffic(kernel: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def _nvtx(torch, name):
+    """Open (name given) or close an NVTX range around a bench phase, for a
+    profiler's timeline; a no-op where NVTX is unavailable."""
+    try:
+        if name is None:
+            torch.cuda.nvtx.range_pop()
+        else:
+            torch.cuda.nvtx.range_push(name)
+    except Exception:
+        pass
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
 
@@ -241,6 +253,7 @@ def run_ours(args, rank, world, dev, torch, dist):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    _nvtx(torch, "timed training steps")
     with ClockSampler(torch.cuda.current_device()) as clk:
         for i in range(args.steps):
             flush.zero_()
@@ -248,6 +261,7 @@ def run_ours(args, rank, world, dev, torch, dist):
             graph.replay()
             ev[i][1].record()
         torch.cuda.synchronize()
+    _nvtx(torch, None)
     if world > 1:
         dist.barrier()
     launches = launches_per_step * args.steps
@@ -354,7 +368,9 @@ def run_ours(args, rank, world, dev, torch, dist):
     torch.cuda.synchronize()
     flush.zero_()
     torch.cuda.synchronize()
+    _nvtx(torch, "end-to-end steps")
     e_ms = e2e_run(args.steps)
+    _nvtx(torch, None)
     if world > 1:
         e_ms = max_over_ranks(e_ms, dist, dev)
     e2e_value = flops_step * args.steps * world / (e_ms * 1e-3) / 1e12
@@ -725,7 +741,9 @@ def main():
     if rank == 0:
         peaks = load_peaks()
         if not args.no_extra:
+            _nvtx(torch, "prefill and decode extras")
             line["extra"] = extra_workloads(torch, dev, args.steps, peaks)
+            _nvtx(torch, None)
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
