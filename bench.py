@@ -627,12 +627,14 @@ def run_reference(args):
 
 
 PROFILE_CASES = ("train", "prefill32k", "prefill262k", "decode", "decode_varlen",
-                 "decode_paged", "prefill32k_noncausal")
+                 "decode_paged", "prefill32k_noncausal", "decode_all")
 
 
 def profile_case(name, warmup):
     """A few untimed calls of one workload, for capturing its kernels with a
-    profiler (no JSON line)."""
+    profiler (no JSON line).  "decode_all" runs the decode, decode_varlen and
+    decode_paged cases in that order on one set of inputs (warmup + 1 calls
+    each)."""
     import torch
     import __graft_entry__
     from transformer_attention_ggd_gb300 import bam_attn as ba
@@ -640,8 +642,9 @@ def profile_case(name, warmup):
 
     __graft_entry__.build()
     dev = torch.device("cuda", torch.cuda.current_device())
+    cases = ("decode", "decode_varlen", "decode_paged") if name == "decode_all" else (name,)
     cfg = {"train": 2, "prefill32k": 3, "prefill262k": 4, "decode": 5, "decode_varlen": 5,
-           "decode_paged": 5, "prefill32k_noncausal": 3}[name]
+           "decode_paged": 5, "prefill32k_noncausal": 3}[cases[0]]
     causal = name != "prefill32k_noncausal"
     d = make_inputs(cfg)
 
@@ -652,7 +655,7 @@ def profile_case(name, warmup):
     prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, causal, True)
     B, H, T = d["B"], d["H"], d["T"]
     q, k, v = bf(d["q"]), bf(d["k"]), bf(d["v"])
-    for _ in range(warmup + 1):
+    for name, _ in ((c, i) for c in cases for i in range(warmup + 1)):
         if name in ("decode_varlen", "decode_paged"):
             lens = np.random.default_rng(5005).integers(1, T + 1, B)
             lens[:3] = [1, T, 64]
@@ -696,7 +699,8 @@ def profile_case(name, warmup):
             ws = ba.workspace(ba.BAM_OP_FWD, B, H, T, dev)
             ba.bam_attn_fwd(q, k, v, o, lse, prm, ws)
     torch.cuda.synchronize()
-    print(f"profile case {name}: {warmup + 1} calls, {ba.bam_attn_launch_count()} launches")
+    print(f"profile case {'+'.join(cases)}: {warmup + 1} calls each, "
+          f"{ba.bam_attn_launch_count()} launches")
 
 
 def main():

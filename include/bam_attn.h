@@ -59,7 +59,8 @@ typedef enum {
   BAM_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. D != 64)        */
   BAM_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed            */
   BAM_ERR_TIMEOUT = 4,     /* a device-side wait gave up (see check_status)   */
-  BAM_ERR_WORKSPACE = 5    /* workspace missing, misaligned or too small      */
+  BAM_ERR_WORKSPACE = 5,   /* workspace missing, misaligned or too small      */
+  BAM_ERR_BOUNDS = 6       /* debug build only: a copy's bounds check failed  */
 } bam_status;
 
 /* Parameterisations of the prior (bam_params.prior). */
@@ -155,8 +156,20 @@ bam_status bam_attn_decode_paged(const void* q, const void* k_pages, const void*
 /* Synchronises `stream`, then reads and clears the device status word of
  * `ws`.  Returns BAM_OK, BAM_ERR_TIMEOUT (a device wait gave up),
  * BAM_ERR_INVALID_ARG (a device-read argument was out of range: a ragged or
- * paged decode's cache length or page number) or BAM_ERR_CUDA. */
+ * paged decode's cache length or page number), BAM_ERR_BOUNDS (debug build:
+ * a bulk copy failed its bounds check and was not issued; the call's outputs
+ * are then invalid) or BAM_ERR_CUDA. */
 bam_status bam_attn_check_status(void* ws, cudaStream_t stream);
+
+/* 1 when the library was built with BAM_DEBUG, else 0.  The debug build is
+ * the same library with every plain bulk copy (the distance-table windows of
+ * the forward and backward, the K, V and table stages of the decode) checked
+ * before it is issued: its source must lie inside its own table row (up to
+ * the padding after the last row), cache row or page, and its addresses and
+ * size must be multiples of 16 bytes.  The row coordinate of every tiled
+ * store and reduction is checked to lie in [0, T).  A failed check records
+ * BAM_ERR_BOUNDS, skips the copy and aborts the call; nothing traps. */
+int bam_attn_debug_build(void);
 
 /* Self-test of the failure detection: launches one thread that waits, with
  * the library's bounded wait, on a barrier nothing arrives at.  After the

@@ -37,9 +37,21 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
-        assert ba.bam_status_string(code)
+    for code in range(7):
+        assert ba.bam_status_string(code) != "unknown status"
     assert ba.bam_status_string(99) == "unknown status"
+
+
+def test_release_and_debug_builds():
+    """The release library reports no debug checks; the BAM_DEBUG build of
+    the same sources exports the same symbols and reports its checks.  Both
+    queries return on the host."""
+    rel = ctypes.CDLL(lib_build.build())
+    dbg = ctypes.CDLL(lib_build.build(debug=True))
+    assert rel.bam_attn_debug_build() == 0
+    assert dbg.bam_attn_debug_build() == 1
+    for name in _declared_functions():
+        assert hasattr(dbg, name), name
 
 
 def test_workspace_sizes(lib):

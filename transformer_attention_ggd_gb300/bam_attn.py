@@ -5,6 +5,11 @@ current CUDA stream; every step of the computation runs in the CUDA kernels
 of libbam_attn.so.  There is no fallback: if the library is missing or no
 GPU is present, calls raise.
 
+With BAM_ATTN_DEBUG=1 in the environment the debug build
+libbam_attn_debug.so is loaded instead (same ABI; every plain bulk copy and
+tiled store is bounds-checked on the device, a failed check is reported by
+bam_attn_check_status as BAM_ERR_BOUNDS).
+
 The functions carry the C names (bam_attn_fwd, bam_attn_bwd, ...).  The
 helpers at the bottom (``attention_forward`` and friends) allocate outputs
 and workspace with torch and then call the same entry points.
@@ -17,7 +22,8 @@ import os
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "_build", "libbam_attn.so")
+DEBUG = os.environ.get("BAM_ATTN_DEBUG", "0") == "1"
+LIB_PATH = os.path.join(PKG, "_build", "libbam_attn_debug.so" if DEBUG else "libbam_attn.so")
 
 BAM_OK = 0
 BAM_ERR_INVALID_ARG = 1
@@ -25,6 +31,7 @@ BAM_ERR_UNSUPPORTED = 2
 BAM_ERR_CUDA = 3
 BAM_ERR_TIMEOUT = 4
 BAM_ERR_WORKSPACE = 5
+BAM_ERR_BOUNDS = 6
 
 BAM_OP_FWD, BAM_OP_BWD, BAM_OP_DECODE = 0, 1, 2
 BAM_PRIOR_ALPHA, BAM_PRIOR_THETA = 0, 1
@@ -52,6 +59,7 @@ EXPORTED = (
     "bam_attn_launch_count",
     "bam_attn_decode_noalloc",
     "bam_attn_selftest_wait",
+    "bam_attn_debug_build",
 )
 
 # Size of the fixed device scratch of bam_attn_decode_noalloc.
@@ -120,6 +128,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bam_attn_decode_noalloc.argtypes = [vp, vp, vp, vp, i, vp, i, i, i, i, pp, vp]
         lib.bam_attn_selftest_wait.restype = i
         lib.bam_attn_selftest_wait.argtypes = [vp, sz, vp]
+        lib.bam_attn_debug_build.restype = i
+        lib.bam_attn_debug_build.argtypes = []
         _lib = lib
         return lib
 
@@ -244,6 +254,11 @@ def bam_attn_selftest_wait(ws, stream=None) -> None:
 
 def bam_attn_check_status(ws, stream=None) -> int:
     return int(load_library().bam_attn_check_status(_ptr(ws), _stream(stream)))
+
+
+def bam_attn_debug_build() -> bool:
+    """True when the loaded library is the bounds-checking debug build."""
+    return bool(load_library().bam_attn_debug_build())
 
 
 def bam_attn_profile_events(which: int, before=None, after=None) -> None:

@@ -3,6 +3,10 @@
 Each .cu translation unit is compiled in parallel, then linked into one
 shared library with a static CUDA runtime.  No cmake, no torch extension
 machinery: the library exports a plain C ABI (include/bam_attn.h).
+
+``build(debug=True)`` makes libbam_attn_debug.so from the same sources with
+BAM_DEBUG defined: device-side bounds checks on every plain bulk copy and
+tiled store, reported through the status word (BAM_ERR_BOUNDS).
 """
 
 from __future__ import annotations
@@ -17,6 +21,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libbam_attn.so")
+DEBUG_BUILD = os.path.join(BUILD, "debug")
+DEBUG_LIB = os.path.join(BUILD, "libbam_attn_debug.so")
 SOURCES = ["api.cu", "table.cu", "fwd.cu", "bwd.cu", "decode.cu", "decode_noalloc.cu",
            "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -43,16 +49,18 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    out_dir, lib = (DEBUG_BUILD, DEBUG_LIB) if debug else (BUILD, LIB)
+    flags = FLAGS + (["-DBAM_DEBUG"] if debug else [])
+    os.makedirs(out_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(ROOT, "include", "bam_attn.h"))
     exe = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         if force or _stale(obj, [os.path.join(CSRC, src)] + headers):
-            cmd = [exe, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj + ".tmp"]
+            cmd = [exe, *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj + ".tmp"]
             if verbose:
                 cmd.append("-Xptxas=-v")
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -65,16 +73,27 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if force or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [exe, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False) -> tuple:
+    """The release and the debug library, built side by side."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        rel = ex.submit(build, force)
+        dbg = ex.submit(build, force, False, True)
+        return rel.result(), dbg.result()
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--debug" in sys.argv:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug=True))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

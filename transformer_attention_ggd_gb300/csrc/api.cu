@@ -431,8 +431,17 @@ bam_status bam_attn_check_status(void* ws, cudaStream_t stream) {
   if (cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return BAM_ERR_CUDA;
   if (cudaMemset(ws, 0, sizeof(st)) != cudaSuccess) return BAM_ERR_CUDA;
   if (st.code == BAM_DEV_BAD_ARG && st.abort == 0) return BAM_ERR_INVALID_ARG;
+  if (st.code == BAM_DEV_BOUNDS) return BAM_ERR_BOUNDS;
   if (st.code != BAM_DEV_OK || st.abort != 0) return BAM_ERR_TIMEOUT;
   return BAM_OK;
+}
+
+int bam_attn_debug_build(void) {
+#ifdef BAM_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 const char* bam_status_string(bam_status s) {
@@ -449,6 +458,8 @@ const char* bam_status_string(bam_status s) {
       return "device-side wait gave up";
     case BAM_ERR_WORKSPACE:
       return "workspace missing, misaligned or too small";
+    case BAM_ERR_BOUNDS:
+      return "a bulk copy failed its bounds check (debug build)";
   }
   return "unknown status";
 }

@@ -33,7 +33,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // copy k = (its row + 1) mod 4 they start on a 16-byte boundary, so one
 // vector load fetches them.  Windows start at multiples of 128 entries.
 constexpr int kTabCopies = 4;
-// Window copies may read up to three entries past the end of a row (never
+// Window copies may read up to four entries past the end of a row (never
 // used); the table region is padded so the last row stays inside it.
 constexpr int kTabPadFloats = 16;
 

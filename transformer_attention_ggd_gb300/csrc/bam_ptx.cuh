@@ -99,7 +99,15 @@ struct DevStatus {
 
 // BAM_DEV_BAD_ARG: an argument only the device reads was out of range (a
 // cache length of the ragged decode); the kernel clamped it and went on.
-enum : int { BAM_DEV_OK = 0, BAM_DEV_TIMEOUT = 1, BAM_DEV_ABORTED = 2, BAM_DEV_BAD_ARG = 3 };
+// BAM_DEV_BOUNDS: a debug build (BAM_DEBUG) found a bulk copy whose source
+// left its buffer or broke the 16-byte rule; the copy was not issued.
+enum : int {
+  BAM_DEV_OK = 0,
+  BAM_DEV_TIMEOUT = 1,
+  BAM_DEV_ABORTED = 2,
+  BAM_DEV_BAD_ARG = 3,
+  BAM_DEV_BOUNDS = 4
+};
 
 // Wall-clock budget of one wait.  Normal waits last microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -107,13 +115,19 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // abort words and the wall clock are still checked often.
 constexpr uint32_t kWaitSleepNs = 20000;  // 20 us
 
-__device__ __forceinline__ void raise_abort(DevStatus* st, volatile int* cta_abort, int site) {
+// Records `code` (the first error of the call wins) and raises the CTA and
+// grid abort words, so that every bounded wait of the grid gives up.
+__device__ __forceinline__ void raise_error(DevStatus* st, volatile int* cta_abort, int site,
+                                            int code) {
   *cta_abort = 1;
-  if (atomicCAS(&st->code, BAM_DEV_OK, BAM_DEV_TIMEOUT) == BAM_DEV_OK) {
+  if (atomicCAS(&st->code, BAM_DEV_OK, code) == BAM_DEV_OK) {
     st->site = site;
     st->block = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
   }
   atomicExch(&st->abort, 1);
+}
+__device__ __forceinline__ void raise_abort(DevStatus* st, volatile int* cta_abort, int site) {
+  raise_error(st, cta_abort, site, BAM_DEV_TIMEOUT);
 }
 
 // Slow path of mbar_wait: spins with a wall-clock limit.
@@ -176,6 +190,66 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Counts `bytes` of an expected transfer as arrived without copying them.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// bulk_load with the checks of a debug build.  With BAM_DEBUG defined, the
+// copy is issued only when its source [src, src + bytes) lies inside
+// [lo, hi) and src, dst and bytes meet the 16-byte rule; otherwise the
+// bytes are counted as arrived on `bar` (so no wait on it hangs), the error
+// BAM_DEV_BOUNDS is recorded with `site`, the grid is aborted and false is
+// returned.  Without BAM_DEBUG this is bulk_load and returns true; the
+// bounds are then unused.
+__device__ __forceinline__ bool bulk_load_checked(void* dst, const void* src, uint32_t bytes,
+                                                  uint64_t* bar, const void* lo, const void* hi,
+                                                  DevStatus* st, volatile int* cta_abort,
+                                                  int site) {
+#ifdef BAM_DEBUG
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
+  const bool inside = s0 >= reinterpret_cast<uintptr_t>(lo) &&
+                      s0 + bytes <= reinterpret_cast<uintptr_t>(hi);
+  const bool aligned16 = ((s0 | smem_u32(dst) | bytes) & 15u) == 0;
+  if (!inside || !aligned16 || bytes == 0) {
+    mbar_complete_tx(bar, bytes);
+    raise_error(st, cta_abort, site, BAM_DEV_BOUNDS);
+    return false;
+  }
+#else
+  (void)lo;
+  (void)hi;
+  (void)st;
+  (void)cta_abort;
+  (void)site;
+#endif
+  bulk_load(dst, src, bytes, bar);
+  return true;
+}
+
+// Debug-build check of the row coordinate of a tiled store or reduction
+// (which must not start at a negative coordinate): records BAM_DEV_BOUNDS
+// and returns false when c1 is outside [0, rows).  Always true without
+// BAM_DEBUG.
+__device__ __forceinline__ bool store_row_ok(int c1, int rows, DevStatus* st,
+                                             volatile int* cta_abort, int site) {
+#ifdef BAM_DEBUG
+  if (c1 < 0 || c1 >= rows) {
+    raise_error(st, cta_abort, site, BAM_DEV_BOUNDS);
+    return false;
+  }
+#else
+  (void)c1;
+  (void)rows;
+  (void)st;
+  (void)cta_abort;
+  (void)site;
+#endif
+  return true;
 }
 
 // Element-wise add of a shared-memory tile into global memory through a 3-D

@@ -108,7 +108,10 @@ enum : int {
   kSiteBWgS = 70,
   kSiteBWgQD = 71,
   kSiteBWgDone = 72,
-  kSiteBWgDq = 73
+  kSiteBWgDq = 73,
+  // Debug-build bounds checks (BAM_DEV_BOUNDS)
+  kSiteBWindowCopy = 74,
+  kSiteBRow = 75
 };
 
 constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 320, kColDK = 384,
@@ -217,6 +220,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
   const uint32_t tm = sm.tmem_base;
   const size_t copy_stride = static_cast<size_t>(a.H) * a.tab_len;  // floats between copies
   const size_t plane = kTabCopies * copy_stride;
+  // End of the three tables and their padding: a window starts inside its
+  // own row and may run past the row's end, never past this.
+  const float* tab_end = a.table + 3 * plane + kTabPadFloats;
 
   // Barrier phases: per query tile g (counted over all items of this CTA)
   // for the Q/dO ring and the tile hand-offs; per item n for K/V.
@@ -249,9 +255,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
                              (a.tab_len - kBWin - (a.tab_off + i0 - it.j0 - 128));
           for (int p = 0; p < 3; ++p)
             for (int k = 0; k < kTabCopies; ++k)
-              bulk_load(sm.win[s][p] + win_copy_off(k, kBWinCopyStride),
-                        src + p * plane + k * copy_stride, kBWinCopy * 4, &sm.qd_full[s]);
+              ok &= bulk_load_checked(
+                  sm.win[s][p] + win_copy_off(k, kBWinCopyStride), src + p * plane + k * copy_stride,
+                  kBWinCopy * 4, &sm.qd_full[s],
+                  a.table + p * plane + k * copy_stride + static_cast<size_t>(it.h) * a.tab_len,
+                  tab_end, a.status, ab, kSiteBWindowCopy);
           issued = g + 1;
+          if (!ok) break;
           if (t == 0) {
             // K and V of the item into the single K/V buffers: V as soon as
             // the previous item's last dP product is done, K after its last
@@ -387,6 +397,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
           ok = mbar_wait(&sm.dqs_full, g & 1, a.status, ab, kSiteBDq);
           if (!ok) break;
           const int i0 = (it.q_first + t) * 128;
+          ok = store_row_ok(i0, a.T, a.status, ab, kSiteBRow);
+          if (!ok) break;
           tma_reduce_add_3d(&tdq, sm.dqs[0], 0, i0, it.bh);
           tma_reduce_add_3d(&tdq, sm.dqs[1], 32, i0, it.bh);
           bulk_commit();
@@ -396,6 +408,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
         if (!ok) break;
         // The item's dK and dV rows (bf16, staged in the P^T buffer).
         ok = mbar_wait(&sm.epi_full, round & 1, a.status, ab, kSiteBDq);
+        if (!ok) break;
+        ok = store_row_ok(it.j0, a.T, a.status, ab, kSiteBRow);
         if (!ok) break;
         tma_store_3d(&tdk, sm.pt, 0, it.j0, it.bh);
         tma_store_3d(&tdv, sm.pt + kTile, 0, it.j0, it.bh);

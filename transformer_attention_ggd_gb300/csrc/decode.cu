@@ -52,7 +52,13 @@ struct __align__(128) DecSmem {
   int abort_flag;
 };
 
-enum : int { kSiteDecProducer = 40, kSiteDecConsumer = 41 };
+enum : int {
+  kSiteDecProducer = 40,
+  kSiteDecConsumer = 41,
+  // Debug-build bounds checks (BAM_DEV_BOUNDS)
+  kSiteDecKV = 42,
+  kSiteDecTable = 43
+};
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& w, float* f) {
   f[0] = __uint_as_float(w.x << 16);
@@ -134,6 +140,7 @@ __global__ void __launch_bounds__(kDecThreads)
         const uint32_t bytes = static_cast<uint32_t>(nk) * kHeadDim * 2;
         mbar_arrive_expect_tx(&sm.full[s], 2 * bytes + kDecTab * 4);
         size_t key0 = row0 + kb;  // first key of the stage, in keys of the cache
+        size_t seg0 = row0, seg1 = row0 + a.Tkv;  // the keys a stage may read
         if (a.block_table) {
           int pg = __ldg(a.block_table + static_cast<size_t>(bh / a.H) * a.max_blocks +
                          kb / a.page);
@@ -141,13 +148,20 @@ __global__ void __launch_bounds__(kDecThreads)
             bad_page = true;
             pg = 0;
           }
-          key0 = (static_cast<size_t>(pg) * a.H + h) * a.page + kb % a.page;
+          seg0 = (static_cast<size_t>(pg) * a.H + h) * a.page;
+          seg1 = seg0 + a.page;  // a stage never crosses a page
+          key0 = seg0 + kb % a.page;
         }
-        bulk_load(sm.k[s], a.kc + key0 * kHeadDim, bytes, &sm.full[s]);
-        bulk_load(sm.v[s], a.vc + key0 * kHeadDim, bytes, &sm.full[s]);
+        ok &= bulk_load_checked(sm.k[s], a.kc + key0 * kHeadDim, bytes, &sm.full[s],
+                                a.kc + seg0 * kHeadDim, a.kc + seg1 * kHeadDim, a.status, ab,
+                                kSiteDecKV);
+        ok &= bulk_load_checked(sm.v[s], a.vc + key0 * kHeadDim, bytes, &sm.full[s],
+                                a.vc + seg0 * kHeadDim, a.vc + seg1 * kHeadDim, a.status, ab,
+                                kSiteDecKV);
         // 16-byte aligned window starting at or below entry kb + tshift
-        bulk_load(sm.tab[s], a.table + static_cast<size_t>(h) * a.tab_len + ((kb + tshift) & ~3),
-                  kDecTab * 4, &sm.full[s]);
+        const float* trow = a.table + static_cast<size_t>(h) * a.tab_len;
+        ok &= bulk_load_checked(sm.tab[s], trow + ((kb + tshift) & ~3), kDecTab * 4, &sm.full[s],
+                                trow, trow + a.tab_len, a.status, ab, kSiteDecTable);
         issued = it + 1;
       }
       for (int it = max(0, issued - kDecStages); it < issued; ++it)

@@ -79,7 +79,10 @@ enum : int {
   kSiteSoftK = 31,
   kSiteSoftPV = 32,
   kSiteSoftEnd = 33,
-  kSiteSoftStore = 34
+  kSiteSoftStore = 34,
+  // Debug-build bounds checks (BAM_DEV_BOUNDS)
+  kSiteWindowCopy = 35,
+  kSiteOutRow = 36
 };
 
 // All lanes wait; the result is made warp-uniform so that the collective
@@ -169,6 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t copy_stride = static_cast<size_t>(a.H) * a.tab_len;
       const float* tab_h = a.table + static_cast<size_t>(h) * a.tab_len +
                            (a.tab_len - kWin - a.tab_off - i0 + 128);
+      // A window starts inside its own row and may run past the row's end
+      // into the padding after the last row, never beyond it.
+      const float* tab_end = a.table + kTabCopies * copy_stride + kTabPadFloats;
       for (int j = 0; ok && j < nKV; ++j) {
         const int s = j % kStages;
         if (j >= kStages) {
@@ -179,8 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sm.k[s], &tk, &sm.k_full[s], 0, 128 * j, bh);
         if (j == 0) grid_dep_wait();  // the windows come from the table kernel
         for (int k = 0; k < kTabCopies; ++k)
-          bulk_load(sm.win[s] + win_copy_off(k, kWinCopyStride), tab_h + k * copy_stride + 128 * j,
-                    kWinCopy * 4, &sm.k_full[s]);
+          ok &= bulk_load_checked(sm.win[s] + win_copy_off(k, kWinCopyStride),
+                                  tab_h + k * copy_stride + 128 * j, kWinCopy * 4, &sm.k_full[s],
+                                  a.table + k * copy_stride + static_cast<size_t>(h) * a.tab_len,
+                                  tab_end, a.status, ab, kSiteWindowCopy);
         mbar_arrive_expect_tx(&sm.v_full[s], kTileBytes);
         tma_load_3d(sm.v[s], &tv, &sm.v_full[s], 0, 128 * j, bh);
         issued = j + 1;
@@ -470,8 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&sm.o_full[t]);
         if ((warp & 3) == 0 && lane == 0) {
           // The tile's first warp stores it once all four have staged.
-          if (mbar_wait(&sm.o_full[t], 0, a.status, ab, kSiteSoftStore)) {
-            const int row0 = i0 + 128 * t;
+          const int row0 = i0 + 128 * t;
+          if (mbar_wait(&sm.o_full[t], 0, a.status, ab, kSiteSoftStore) &&
+              store_row_ok(row0, a.T, a.status, ab, kSiteOutRow)) {
             if (a.o_fp32) {
               tma_store_3d(&to, sm.ost[t], 0, row0, bh);
               tma_store_3d(&to, sm.ost[t] + kTileBytes, 32, row0, bh);
