@@ -203,7 +203,7 @@ def run_ours(args, rank, world, dev, torch, dist):
     ba.load_library()
     peaks = load_peaks()
     B, H, T = 8, 12, 512
-    d, t = make_train_inputs(torch, dev, seed=1002 + rank)
+    d, t = make_train_inputs(torch, dev, seed=args.seed + rank)
     prm = ba.make_params(t["alpha"], t["beta"], t["mu"], t["s"], 1e-5, True, True)
     o = torch.empty((B, H, T, D), dtype=torch.float32, device=dev)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
@@ -407,6 +407,7 @@ def run_ours(args, rank, world, dev, torch, dist):
                    "causal": True, "ssmax": True, "step": "fwd+bwd",
                    "l2": "flushed (256 MB write) between timed steps",
                    "launch": "CUDA graph of the two C-ABI calls, replayed per step",
+                   "seed": f"{args.seed} + rank",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -582,11 +583,11 @@ def oracle_sample_step(d, nbh, nthreads):
     return dt, train_flops(bsel, hsel, T)
 
 
-def cpu_baseline(nbh=96):
+def cpu_baseline(nbh=96, seed=1002):
     from transformer_attention_ggd_gb300.inputs import make_inputs
     import oracle
     oracle.build()
-    d = make_inputs(2)
+    d = make_inputs(2, seed=seed)
     cores = os.cpu_count() or 1
     dt, fl = oracle_sample_step(d, nbh, cores)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
@@ -599,7 +600,7 @@ def run_reference(args):
     from transformer_attention_ggd_gb300.inputs import make_inputs
     import oracle
     oracle.build()
-    d = make_inputs(2)
+    d = make_inputs(2, seed=args.seed)
     cores = os.cpu_count() or 1
     nbh = 96
     for _ in range(args.warmup):
@@ -711,6 +712,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip prefill/decode extras")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--seed", type=int, default=1002,
+                    help="seed of the training-step inputs (rank r draws with seed + r)")
     ap.add_argument("--profile-case", choices=PROFILE_CASES,
                     help="only run a few untimed calls of one workload (for profilers)")
     args = ap.parse_args()
@@ -749,7 +752,7 @@ def main():
             line["extra"] = extra_workloads(torch, dev, args.steps, peaks)
             _nvtx(torch, None)
         if not args.no_cpu:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(seed=args.seed)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -41,6 +41,11 @@
  *  - Every on-device wait is bounded.  A kernel that gives up records
  *    BAM_ERR_TIMEOUT in the workspace status word and returns; read it with
  *    bam_attn_check_status().
+ *  - One device per process (one process per GPU, as torch.distributed
+ *    launches ranks): the kernels' shared-memory limits are raised once, on
+ *    the device current at the first call.  On another device of the same
+ *    process the launch of the first kernel that needs the raised limit is
+ *    refused and the call returns BAM_ERR_CUDA.
  */
 #ifndef BAM_ATTN_H_
 #define BAM_ATTN_H_
