@@ -110,6 +110,22 @@ def profiled_traffic(kernel: str):
     return entry.get("dram_bytes_per_launch")
 
 
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed
+    captures: the entry `kernel` or `kernel@workload` whose workload matches,
+    if it was taken on the current sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    for key in (kernel, f"{kernel}@{workload}"):
+        entry = t.get(key)
+        if entry and entry.get("workload") == workload:
+            return profiled_traffic(key)
+    return None
+
+
 def _nvtx(torch, name):
     """Open (name given) or close an NVTX range around a bench phase, for a
     profiler's timeline; a no-op where NVTX is unavailable."""
@@ -387,8 +403,8 @@ def run_ours(args, rank, world, dev, torch, dist):
     roof = {"kernel": "bam_bwd_kernel" if dom == ba.BAM_KERNEL_BWD else "bam_fwd_kernel",
             "bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
             "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic("bam_bwd_kernel" if dom == ba.BAM_KERNEL_BWD
-                                        else "bam_fwd_kernel"),
+            "traffic": traffic_for("bam_bwd_kernel" if dom == ba.BAM_KERNEL_BWD
+                                   else "bam_fwd_kernel", f"train_B{B}_H{H}_T{T}"),
             "peak_source": f"{peaks['source']} bf16 burst (cuBLAS)",
             "kernel_ms": {"table": round(kern_ms[ba.BAM_KERNEL_TABLE], 4),
                           "fwd": round(kern_ms[ba.BAM_KERNEL_FWD], 4),
@@ -460,10 +476,12 @@ def extra_workloads(torch, dev, steps, peaks):
         fl = (pairs_causal(B, H, T) if causal else B * H * T * T) * 4 * D
         tf = fl / (statistics.median(ms) * 1e-3) / 1e12
         ktf = fl / (statistics.median(kms) * 1e-3) / 1e12
-        out[f"prefill_{'' if causal else 'noncausal_'}B{B}_H{H}_T{T}"] = {
+        name = f"prefill_{'' if causal else 'noncausal_'}B{B}_H{H}_T{T}"
+        out[name] = {
             "ms": round(statistics.median(ms), 4), "TFLOP/s": round(tf, 2),
             "fwd_kernel_TFLOP/s": round(ktf, 2),
-            "frac_of_bf16_peak": round(ktf / peaks["bf16_tflops"], 4)}
+            "frac_of_bf16_peak": round(ktf / peaks["bf16_tflops"], 4),
+            "traffic": traffic_for("bam_fwd_kernel", name)}
         del q, k, v, o, ws
         torch.cuda.empty_cache()
 
@@ -492,9 +510,11 @@ def extra_workloads(torch, dev, steps, peaks):
     kv_bytes = 2 * B * H * Tkv * D * 2
     gbs = kv_bytes / (statistics.median(ms) * 1e-3) / 1e9
     kgbs = kv_bytes / (statistics.median(kms) * 1e-3) / 1e9
-    out[f"decode_B{B}_H{H}_Tkv{Tkv}"] = {
+    name = f"decode_B{B}_H{H}_Tkv{Tkv}"
+    out[name] = {
         "ms": round(statistics.median(ms), 4), "GB/s": round(gbs, 1),
-        "decode_kernel_GB/s": round(kgbs, 1), "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4)}
+        "decode_kernel_GB/s": round(kgbs, 1), "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4),
+        "traffic": traffic_for("bam_decode_kernel", name)}
 
     # Ragged decode on the same cache: seeded lengths U[1, Tkv] per sequence;
     # the bytes are those of the keys each sequence actually holds.
@@ -518,10 +538,12 @@ def extra_workloads(torch, dev, steps, peaks):
     kv_bytes = 2 * int(lens.sum()) * H * D * 2
     gbs = kv_bytes / (statistics.median(ms) * 1e-3) / 1e9
     kgbs = kv_bytes / (statistics.median(kms) * 1e-3) / 1e9
-    out[f"decode_varlen_B{B}_H{H}_Tmax{Tkv}"] = {
+    name = f"decode_varlen_B{B}_H{H}_Tmax{Tkv}"
+    out[name] = {
         "ms": round(statistics.median(ms), 4), "mean_len": round(float(lens.mean()), 1),
         "GB/s": round(gbs, 1), "decode_kernel_GB/s": round(kgbs, 1),
-        "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4)}
+        "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4),
+        "traffic": traffic_for("bam_decode_kernel", name)}
 
     # Paged decode: the same ragged cache in 256-key pages, randomly permuted
     # (page p of the [B * Tkv/256] blocks stored at slot perm[p]).
@@ -552,10 +574,12 @@ def extra_workloads(torch, dev, steps, peaks):
         raise RuntimeError("paged decode status not clean")
     gbs = kv_bytes / (statistics.median(ms) * 1e-3) / 1e9
     kgbs = kv_bytes / (statistics.median(kms) * 1e-3) / 1e9
-    out[f"decode_paged{page}_B{B}_H{H}_Tmax{Tkv}"] = {
+    name = f"decode_paged{page}_B{B}_H{H}_Tmax{Tkv}"
+    out[name] = {
         "ms": round(statistics.median(ms), 4), "mean_len": round(float(lens.mean()), 1),
         "GB/s": round(gbs, 1), "decode_kernel_GB/s": round(kgbs, 1),
-        "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4)}
+        "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4),
+        "traffic": traffic_for("bam_decode_kernel", name)}
     del pools
     torch.cuda.empty_cache()
     return out

@@ -85,6 +85,25 @@ def test_traffic_is_dropped_once_the_sources_change(tmp_path, monkeypatch):
     assert bench.profiled_traffic("bam_decode_kernel") is None   # never captured
 
 
+def test_traffic_is_matched_to_its_workload(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    os.symlink(os.path.join(ROOT, "transformer_attention_ggd_gb300"),
+               tmp_path / "transformer_attention_ggd_gb300")
+    h = bench.kernel_source_hash("bam_fwd_kernel")
+    entries = {
+        "bam_fwd_kernel": {"workload": "prefill_A", "source_hash": h,
+                           "dram_bytes_per_launch": 1},
+        "bam_fwd_kernel@train_B": {"workload": "train_B", "source_hash": h,
+                                   "dram_bytes_per_launch": 2},
+    }
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(entries))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_for("bam_fwd_kernel", "prefill_A") == 1
+    assert bench.traffic_for("bam_fwd_kernel", "train_B") == 2
+    assert bench.traffic_for("bam_fwd_kernel", "prefill_C") is None
+    assert bench.traffic_for("bam_bwd_kernel", "train_B") is None
+
+
 def test_clock_summary():
     cs = bench.ClockSampler(0)
     cs.lines = [
