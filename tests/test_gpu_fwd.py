@@ -174,3 +174,36 @@ def test_repeat_calls_identical():
     o2, l2 = _run(bits, prm, True, True)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+def test_binding_refuses_bad_tensors_then_runs():
+    """A tensor of the wrong shape, dtype or layout is refused before any
+    launch; the next good call on the same workspace is correct."""
+    rng = np.random.default_rng(31)
+    B, H, T = 1, 2, 130
+    bits = {n: normal_bits(rng, (B, H, T, 64)) for n in "qkv"}
+    prm_np = random_params(H, rng, mu_hi=3.0)
+    q, k, v = (dev_bf16(bits[n]) for n in "qkv")
+    t = params_dev(prm_np)
+    prm = ba.make_params(t["alpha"], t["beta"], t["mu"], t["s"], 1e-5, True, True)
+    o = torch.empty((B, H, T, 64), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, H, T), dtype=torch.float32, device="cuda")
+    ws = ba.workspace(ba.BAM_OP_FWD, B, H, T)
+    k_strided = torch.empty((B, H, 64, T), dtype=torch.bfloat16, device="cuda").transpose(2, 3)
+    n0 = ba.bam_attn_launch_count()
+    with pytest.raises(ValueError, match="contiguous"):
+        ba.bam_attn_fwd(q, k_strided, v, o, lse, prm, ws)
+    with pytest.raises(ValueError, match="shape"):
+        ba.bam_attn_fwd(q, k[:, :, :-1], v, o, lse, prm, ws)
+    with pytest.raises(ValueError, match="dtype"):
+        ba.bam_attn_fwd(q, k, v.float(), o, lse, prm, ws)
+    with pytest.raises(ValueError, match="ws"):
+        ba.bam_attn_fwd(q, k, v, o, lse, prm, ws.view(torch.int32))
+    with pytest.raises(ValueError, match="shape"):
+        ba.bam_attn_fwd(q[:, :1].contiguous(), k[:, :1].contiguous(), v[:, :1].contiguous(),
+                        o[:, :1].contiguous(), lse[:, :1].contiguous(), prm, ws)
+    assert ba.bam_attn_launch_count() == n0
+    ba.bam_attn_fwd(q, k, v, o, lse, prm, ws)
+    assert ba.bam_attn_check_status(ws) == ba.BAM_OK
+    oref, _ = _oracle(bits, prm_np, True, True)
+    np.testing.assert_allclose(o.cpu().numpy(), oref, rtol=0, atol=O_ATOL)

@@ -149,11 +149,82 @@ def _stream(stream):
 
 def make_params(alpha, beta, mu, s=None, eps=1e-5, causal=True, ssmax=False,
                 prior=BAM_PRIOR_ALPHA) -> BamParams:
-    """alpha, beta, mu, s: float32 CUDA tensors of length H (kept alive by the caller).
-    prior: BAM_PRIOR_ALPHA, or BAM_PRIOR_THETA when alpha, beta, mu hold the thetas."""
-    return BamParams(alpha.data_ptr(), beta.data_ptr(), mu.data_ptr(),
-                     s.data_ptr() if s is not None else None, float(eps), int(bool(causal)),
-                     int(bool(ssmax)), int(prior))
+    """alpha, beta, mu, s: contiguous float32 CUDA tensors of length H, which
+    the returned struct keeps alive.  prior: BAM_PRIOR_ALPHA, or
+    BAM_PRIOR_THETA when alpha, beta, mu hold the thetas."""
+    import torch
+    if not isinstance(alpha, torch.Tensor) or alpha.dim() != 1:
+        raise ValueError("alpha must be a 1-D tensor of length H")
+    H = alpha.shape[0]
+    for name, t in (("alpha", alpha), ("beta", beta), ("mu", mu), ("s", s)):
+        _require(t, name, (H,), (torch.float32,), alpha.device, optional=name == "s")
+    if ssmax and s is None:
+        raise ValueError("ssmax needs the per-head scale s")
+    prm = BamParams(alpha.data_ptr(), beta.data_ptr(), mu.data_ptr(),
+                    s.data_ptr() if s is not None else None, float(eps), int(bool(causal)),
+                    int(bool(ssmax)), int(prior))
+    prm.tensors = (alpha, beta, mu, s)
+    return prm
+
+
+# ---------------------------------------------------------------- argument checks
+# The C ABI sees raw pointers and sizes only; these checks keep a tensor of
+# the wrong shape, dtype, device or layout from reaching the kernels, which
+# would read or write outside its storage.
+
+def _require(t, name, shape, dtypes, device, optional=False):
+    import torch
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if (t.dtype in dtypes and t.shape == shape and t.is_contiguous()
+            and t.device == device):
+        return
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _device(q):
+    """The CUDA device of q, which must be the current device (the library
+    launches there, on that device's stream)."""
+    import torch
+    if not isinstance(q, torch.Tensor) or not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor")
+    if q.device.index != torch.cuda.current_device():
+        raise ValueError(f"q is on {q.device}, but cuda:{torch.cuda.current_device()} is "
+                         "the current device")
+    return q.device
+
+
+def _check_params(params: BamParams, H: int, device):
+    import torch
+    tensors = getattr(params, "tensors", None)
+    if tensors is None:
+        return  # built by hand from raw pointers: the caller vouches for them
+    for name, t in zip(("alpha", "beta", "mu", "s"), tensors):
+        _require(t, name, (H,), (torch.float32,), device, optional=name == "s")
+
+
+def _check_ws(ws, device):
+    import torch
+    if not isinstance(ws, torch.Tensor) or ws.dtype != torch.uint8 or ws.dim() != 1:
+        raise ValueError("ws must be a 1-D uint8 tensor (see workspace())")
+    if ws.device != device or not ws.is_contiguous():
+        raise ValueError(f"ws must be a contiguous tensor on {device}")
+
+
+def _out_dtypes():
+    import torch
+    return (torch.float32, torch.bfloat16)
 
 
 def _check(status: int, where: str):
@@ -171,7 +242,15 @@ def bam_attn_workspace_size(op: int, B: int, H: int, T: int, D: int = 64) -> int
 
 def bam_attn_fwd(q, k, v, o, lse, params: BamParams, ws, stream=None) -> None:
     import torch
+    dev = _device(q)
     B, H, T, D = q.shape
+    bf = (torch.bfloat16,)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, (B, H, T, D), bf, dev)
+    _require(o, "o", (B, H, T, D), _out_dtypes(), dev)
+    _require(lse, "lse", (B, H, T), (torch.float32,), dev, optional=True)
+    _check_params(params, H, dev)
+    _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), o_fp32, _ptr(lse), B, H,
                                      T, D, ctypes.byref(params), _ptr(ws), ws.numel(),
@@ -182,7 +261,18 @@ def bam_attn_fwd(q, k, v, o, lse, params: BamParams, ws, stream=None) -> None:
 def bam_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, dalpha, dbeta, dmu, ds, params: BamParams,
                  ws, stream=None) -> None:
     import torch
+    dev = _device(q)
     B, H, T, D = q.shape
+    bf = (torch.bfloat16,)
+    for name, t in (("q", q), ("k", k), ("v", v), ("dO", dO), ("dq", dq), ("dk", dk),
+                    ("dv", dv)):
+        _require(t, name, (B, H, T, D), bf, dev)
+    _require(o, "o", (B, H, T, D), _out_dtypes(), dev)
+    _require(lse, "lse", (B, H, T), (torch.float32,), dev)
+    for name, t in (("dalpha", dalpha), ("dbeta", dbeta), ("dmu", dmu), ("ds", ds)):
+        _require(t, name, (H,), (torch.float32,), dev)
+    _check_params(params, H, dev)
+    _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), o_fp32, _ptr(lse),
                                      _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
@@ -192,9 +282,22 @@ def bam_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, dalpha, dbeta, dmu, ds, params
     _check(st, "bam_attn_bwd")
 
 
+def _check_decode_qo(q, o, lse, B, H, D, dev):
+    import torch
+    _require(q, "q", (B, H, D), (torch.bfloat16,), dev)
+    _require(o, "o", (B, H, D), _out_dtypes(), dev)
+    _require(lse, "lse", (B, H), (torch.float32,), dev, optional=True)
+
+
 def bam_attn_decode(q, kc, vc, o, lse, params: BamParams, ws, stream=None) -> None:
     import torch
+    dev = _device(q)
     B, H, Tkv, D = kc.shape
+    for name, t in (("kc", kc), ("vc", vc)):
+        _require(t, name, (B, H, Tkv, D), (torch.bfloat16,), dev)
+    _check_decode_qo(q, o, lse, B, H, D, dev)
+    _check_params(params, H, dev)
+    _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(o), o_fp32, _ptr(lse),
                                         B, H, Tkv, D, ctypes.byref(params), _ptr(ws), ws.numel(),
@@ -206,7 +309,14 @@ def bam_attn_decode_varlen(q, kc, vc, cache_lens, o, lse, params: BamParams, ws,
                            stream=None) -> None:
     """cache_lens: int32 CUDA tensor [B] (each in [1, Tmax]); kc, vc: [B,H,Tmax,64]."""
     import torch
+    dev = _device(q)
     B, H, Tmax, D = kc.shape
+    for name, t in (("kc", kc), ("vc", vc)):
+        _require(t, name, (B, H, Tmax, D), (torch.bfloat16,), dev)
+    _require(cache_lens, "cache_lens", (B,), (torch.int32,), dev)
+    _check_decode_qo(q, o, lse, B, H, D, dev)
+    _check_params(params, H, dev)
+    _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_decode_varlen(_ptr(q), _ptr(kc), _ptr(vc), _ptr(cache_lens),
                                                _ptr(o), o_fp32, _ptr(lse), B, H, Tmax, D,
@@ -220,8 +330,16 @@ def bam_attn_decode_paged(q, k_pages, v_pages, block_table, cache_lens, o, lse,
     """k_pages, v_pages: [num_pages, H, page, 64]; block_table int32 [B, max_blocks];
     cache_lens int32 [B]."""
     import torch
+    dev = _device(q)
     num_pages, H, page, D = k_pages.shape
     B, max_blocks = block_table.shape
+    for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
+        _require(t, name, (num_pages, H, page, D), (torch.bfloat16,), dev)
+    _require(block_table, "block_table", (B, max_blocks), (torch.int32,), dev)
+    _require(cache_lens, "cache_lens", (B,), (torch.int32,), dev)
+    _check_decode_qo(q, o, lse, B, H, D, dev)
+    _check_params(params, H, dev)
+    _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages),
                                               _ptr(block_table), _ptr(cache_lens), _ptr(o),
@@ -237,7 +355,12 @@ def bam_attn_decode_noalloc(q, kc, vc, o, lse, params: BamParams, stream=None) -
     cudaMalloc's possible synchronisation): no workspace argument, scratch
     from the library's fixed device array.  Overlapping calls race."""
     import torch
+    dev = _device(q)
     B, H, Tkv, D = kc.shape
+    for name, t in (("kc", kc), ("vc", vc)):
+        _require(t, name, (B, H, Tkv, D), (torch.bfloat16,), dev)
+    _check_decode_qo(q, o, lse, B, H, D, dev)
+    _check_params(params, H, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_decode_noalloc(_ptr(q), _ptr(kc), _ptr(vc), _ptr(o), o_fp32,
                                                 _ptr(lse), B, H, Tkv, D, ctypes.byref(params),
