@@ -25,10 +25,12 @@ D_HEAD = 64
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
-    """float32 -> bf16 bit patterns (uint16), round to nearest even."""
+    """float32 -> bf16 bit patterns (uint16), round to nearest even; a NaN
+    stays a (quiet) NaN instead of rounding into the infinity pattern."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     u = x.view(np.uint32).astype(np.uint64)
     rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    rounded = np.where(np.isnan(x), (u >> 16) | 0x40, rounded)
     return rounded.astype(np.uint16)
 
 
