@@ -27,13 +27,16 @@ def lib_path() -> str:
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle (plain g++, no fast-math) if missing or stale."""
+    """Compile the oracle (plain g++, no fast-math, no FMA contraction: each
+    expression rounds as written, the same on x86-64 and aarch64) if missing
+    or stale."""
     os.makedirs(_BUILD, exist_ok=True)
-    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < max(
+        os.path.getmtime(_SRC), os.path.getmtime(__file__))  # source or flags changed
     if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
-               "-fno-fast-math", "-o", tmp, _SRC]
+               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
