@@ -330,7 +330,7 @@ def run_ours(args, rank, world, dev, torch, dist):
     # copy engines.
     s_h2d2, s_d2h2 = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_run(K):
+    def e2e_run(K, check):
         ev_in = [torch.cuda.Event() for _ in range(nb)]
         ev_in2 = [torch.cuda.Event() for _ in range(nb)]
         ev_cmp = [torch.cuda.Event() for _ in range(nb)]
@@ -361,9 +361,9 @@ def run_ours(args, rank, world, dev, torch, dist):
                         s_cmp.wait_event(ev_out2[b])
                     (gq, gk, gv), gs = dev_out[b]
                     x = dev_in[b]
-                    ba.bam_attn_fwd(x["q"], x["k"], x["v"], o, lse, prm, ws_f)
+                    ba.bam_attn_fwd(x["q"], x["k"], x["v"], o, lse, prm, ws_f, check=check)
                     ba.bam_attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], gq, gk, gv,
-                                    gs[0], gs[1], gs[2], gs[3], prm, ws_b)
+                                    gs[0], gs[1], gs[2], gs[3], prm, ws_b, check=check)
                     ev_cmp[b].record(s_cmp)
             if 2 <= i <= K + 1:  # D2H of step i-2
                 b = (i - 2) % nb
@@ -380,12 +380,14 @@ def run_ours(args, rank, world, dev, torch, dist):
         t1.synchronize()
         return t0.elapsed_time(t1)
 
-    e2e_run(max(3, args.warmup))
+    # The warm-up pass checks every buffer (and fails loudly on a bad one);
+    # the timed pass reuses the same preallocated buffers with check=False.
+    e2e_run(max(3, args.warmup), check=True)
     torch.cuda.synchronize()
     flush.zero_()
     torch.cuda.synchronize()
     _nvtx(torch, "end-to-end steps")
-    e_ms = e2e_run(args.steps)
+    e_ms = e2e_run(args.steps, check=False)
     _nvtx(torch, None)
     if world > 1:
         e_ms = max_over_ranks(e_ms, dist, dev)
@@ -431,7 +433,8 @@ def run_ours(args, rank, world, dev, torch, dist):
                 "mode": "streamed: each step's pinned-host H2D of q, k, v, dO and D2H of "
                         "dq, dk, dv and the scalar gradients, overlapping the neighbouring "
                         "steps' kernels (double-buffered, two copy streams per direction, "
-                        "eager C-ABI calls)"},
+                        "eager C-ABI calls; tensor checks on the warm-up pass, check=False "
+                        "on the timed pass over the same preallocated buffers)"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }

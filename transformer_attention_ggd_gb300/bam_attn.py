@@ -5,6 +5,11 @@ current CUDA stream; every step of the computation runs in the CUDA kernels
 of libbam_attn.so.  There is no fallback: if the library is missing or no
 GPU is present, calls raise.
 
+The entry points check every tensor argument (CUDA, current device,
+contiguous, the dtype and shape the call implies) before the call and raise
+ValueError; ``check=False`` skips that for buffers a caller has already
+passed through a checked call (a loop over preallocated tensors).
+
 With BAM_ATTN_DEBUG=1 in the environment the debug build
 libbam_attn_debug.so is loaded instead (same ABI; every plain bulk copy and
 tiled store is bounds-checked on the device, a failed check is reported by
@@ -205,13 +210,49 @@ def _device(q):
     return q.device
 
 
-def _check_params(params: BamParams, H: int, device):
-    import torch
+_DTYPES = None
+
+
+def _dt():
+    """The dtype tuples the entry points accept: bf16, fp32, an output (fp32
+    or bf16) and int32."""
+    global _DTYPES
+    if _DTYPES is None:
+        import torch
+        _DTYPES = ((torch.bfloat16,), (torch.float32,), (torch.float32, torch.bfloat16),
+                   (torch.int32,))
+    return _DTYPES
+
+
+def _check_tensors(specs, device):
+    """specs: (name, tensor, shape, dtypes, optional) per argument.  One quick
+    pass over all of them; only when one fails does the detailed pass run,
+    which raises for the first bad argument."""
+    for name, t, shape, dtypes, optional in specs:
+        if t is None:
+            if optional:
+                continue
+            break
+        try:
+            if not (t.dtype in dtypes and t.shape == shape and t.is_contiguous()
+                    and t.device == device):
+                break
+        except AttributeError:
+            break
+    else:
+        return
+    for name, t, shape, dtypes, optional in specs:
+        _require(t, name, shape, dtypes, device, optional)
+    raise ValueError("argument check failed")
+
+
+def _param_specs(params: BamParams, H: int):
     tensors = getattr(params, "tensors", None)
     if tensors is None:
-        return  # built by hand from raw pointers: the caller vouches for them
-    for name, t in zip(("alpha", "beta", "mu", "s"), tensors):
-        _require(t, name, (H,), (torch.float32,), device, optional=name == "s")
+        return ()  # built by hand from raw pointers: the caller vouches for them
+    f32 = _dt()[1]
+    return tuple((n, t, (H,), f32, n == "s")
+                 for n, t in zip(("alpha", "beta", "mu", "s"), tensors))
 
 
 def _check_ws(ws, device):
@@ -220,11 +261,6 @@ def _check_ws(ws, device):
         raise ValueError("ws must be a 1-D uint8 tensor (see workspace())")
     if ws.device != device or not ws.is_contiguous():
         raise ValueError(f"ws must be a contiguous tensor on {device}")
-
-
-def _out_dtypes():
-    import torch
-    return (torch.float32, torch.bfloat16)
 
 
 def _check(status: int, where: str):
@@ -240,17 +276,17 @@ def bam_attn_workspace_size(op: int, B: int, H: int, T: int, D: int = 64) -> int
     return int(load_library().bam_attn_workspace_size(op, B, H, T, D))
 
 
-def bam_attn_fwd(q, k, v, o, lse, params: BamParams, ws, stream=None) -> None:
+def bam_attn_fwd(q, k, v, o, lse, params: BamParams, ws, stream=None, check=True) -> None:
     import torch
-    dev = _device(q)
     B, H, T, D = q.shape
-    bf = (torch.bfloat16,)
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _require(t, name, (B, H, T, D), bf, dev)
-    _require(o, "o", (B, H, T, D), _out_dtypes(), dev)
-    _require(lse, "lse", (B, H, T), (torch.float32,), dev, optional=True)
-    _check_params(params, H, dev)
-    _check_ws(ws, dev)
+    if check:
+        dev = _device(q)
+        bf, f32, out, _ = _dt()
+        x4 = (B, H, T, D)
+        _check_tensors((("q", q, x4, bf, False), ("k", k, x4, bf, False), ("v", v, x4, bf, False),
+                        ("o", o, x4, out, False), ("lse", lse, (B, H, T), f32, True))
+                       + _param_specs(params, H), dev)
+        _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), o_fp32, _ptr(lse), B, H,
                                      T, D, ctypes.byref(params), _ptr(ws), ws.numel(),
@@ -259,20 +295,21 @@ def bam_attn_fwd(q, k, v, o, lse, params: BamParams, ws, stream=None) -> None:
 
 
 def bam_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, dalpha, dbeta, dmu, ds, params: BamParams,
-                 ws, stream=None) -> None:
+                 ws, stream=None, check=True) -> None:
     import torch
-    dev = _device(q)
     B, H, T, D = q.shape
-    bf = (torch.bfloat16,)
-    for name, t in (("q", q), ("k", k), ("v", v), ("dO", dO), ("dq", dq), ("dk", dk),
-                    ("dv", dv)):
-        _require(t, name, (B, H, T, D), bf, dev)
-    _require(o, "o", (B, H, T, D), _out_dtypes(), dev)
-    _require(lse, "lse", (B, H, T), (torch.float32,), dev)
-    for name, t in (("dalpha", dalpha), ("dbeta", dbeta), ("dmu", dmu), ("ds", ds)):
-        _require(t, name, (H,), (torch.float32,), dev)
-    _check_params(params, H, dev)
-    _check_ws(ws, dev)
+    if check:
+        dev = _device(q)
+        bf, f32, out, _ = _dt()
+        x4 = (B, H, T, D)
+        _check_tensors(tuple((n, t, x4, bf, False) for n, t in (
+                           ("q", q), ("k", k), ("v", v), ("dO", dO), ("dq", dq), ("dk", dk),
+                           ("dv", dv)))
+                       + (("o", o, x4, out, False), ("lse", lse, (B, H, T), f32, False))
+                       + tuple((n, t, (H,), f32, False) for n, t in (
+                           ("dalpha", dalpha), ("dbeta", dbeta), ("dmu", dmu), ("ds", ds)))
+                       + _param_specs(params, H), dev)
+        _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), o_fp32, _ptr(lse),
                                      _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dalpha),
@@ -282,22 +319,22 @@ def bam_attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, dalpha, dbeta, dmu, ds, params
     _check(st, "bam_attn_bwd")
 
 
-def _check_decode_qo(q, o, lse, B, H, D, dev):
-    import torch
-    _require(q, "q", (B, H, D), (torch.bfloat16,), dev)
-    _require(o, "o", (B, H, D), _out_dtypes(), dev)
-    _require(lse, "lse", (B, H), (torch.float32,), dev, optional=True)
+def _decode_specs(q, o, lse, B, H, D):
+    bf, f32, out, _ = _dt()
+    return (("q", q, (B, H, D), bf, False), ("o", o, (B, H, D), out, False),
+            ("lse", lse, (B, H), f32, True))
 
 
-def bam_attn_decode(q, kc, vc, o, lse, params: BamParams, ws, stream=None) -> None:
+def bam_attn_decode(q, kc, vc, o, lse, params: BamParams, ws, stream=None, check=True) -> None:
     import torch
-    dev = _device(q)
     B, H, Tkv, D = kc.shape
-    for name, t in (("kc", kc), ("vc", vc)):
-        _require(t, name, (B, H, Tkv, D), (torch.bfloat16,), dev)
-    _check_decode_qo(q, o, lse, B, H, D, dev)
-    _check_params(params, H, dev)
-    _check_ws(ws, dev)
+    if check:
+        dev = _device(q)
+        bf = _dt()[0]
+        kv = (B, H, Tkv, D)
+        _check_tensors((("kc", kc, kv, bf, False), ("vc", vc, kv, bf, False))
+                       + _decode_specs(q, o, lse, B, H, D) + _param_specs(params, H), dev)
+        _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(o), o_fp32, _ptr(lse),
                                         B, H, Tkv, D, ctypes.byref(params), _ptr(ws), ws.numel(),
@@ -306,17 +343,18 @@ def bam_attn_decode(q, kc, vc, o, lse, params: BamParams, ws, stream=None) -> No
 
 
 def bam_attn_decode_varlen(q, kc, vc, cache_lens, o, lse, params: BamParams, ws,
-                           stream=None) -> None:
+                           stream=None, check=True) -> None:
     """cache_lens: int32 CUDA tensor [B] (each in [1, Tmax]); kc, vc: [B,H,Tmax,64]."""
     import torch
-    dev = _device(q)
     B, H, Tmax, D = kc.shape
-    for name, t in (("kc", kc), ("vc", vc)):
-        _require(t, name, (B, H, Tmax, D), (torch.bfloat16,), dev)
-    _require(cache_lens, "cache_lens", (B,), (torch.int32,), dev)
-    _check_decode_qo(q, o, lse, B, H, D, dev)
-    _check_params(params, H, dev)
-    _check_ws(ws, dev)
+    if check:
+        dev = _device(q)
+        bf, _, _, i32 = _dt()
+        _check_tensors((("kc", kc, (B, H, Tmax, D), bf, False),
+                        ("vc", vc, (B, H, Tmax, D), bf, False),
+                        ("cache_lens", cache_lens, (B,), i32, False))
+                       + _decode_specs(q, o, lse, B, H, D) + _param_specs(params, H), dev)
+        _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_decode_varlen(_ptr(q), _ptr(kc), _ptr(vc), _ptr(cache_lens),
                                                _ptr(o), o_fp32, _ptr(lse), B, H, Tmax, D,
@@ -326,20 +364,22 @@ def bam_attn_decode_varlen(q, kc, vc, cache_lens, o, lse, params: BamParams, ws,
 
 
 def bam_attn_decode_paged(q, k_pages, v_pages, block_table, cache_lens, o, lse,
-                          params: BamParams, ws, stream=None) -> None:
+                          params: BamParams, ws, stream=None, check=True) -> None:
     """k_pages, v_pages: [num_pages, H, page, 64]; block_table int32 [B, max_blocks];
     cache_lens int32 [B]."""
     import torch
-    dev = _device(q)
     num_pages, H, page, D = k_pages.shape
     B, max_blocks = block_table.shape
-    for name, t in (("k_pages", k_pages), ("v_pages", v_pages)):
-        _require(t, name, (num_pages, H, page, D), (torch.bfloat16,), dev)
-    _require(block_table, "block_table", (B, max_blocks), (torch.int32,), dev)
-    _require(cache_lens, "cache_lens", (B,), (torch.int32,), dev)
-    _check_decode_qo(q, o, lse, B, H, D, dev)
-    _check_params(params, H, dev)
-    _check_ws(ws, dev)
+    if check:
+        dev = _device(q)
+        bf, _, _, i32 = _dt()
+        pages = (num_pages, H, page, D)
+        _check_tensors((("k_pages", k_pages, pages, bf, False),
+                        ("v_pages", v_pages, pages, bf, False),
+                        ("block_table", block_table, (B, max_blocks), i32, False),
+                        ("cache_lens", cache_lens, (B,), i32, False))
+                       + _decode_specs(q, o, lse, B, H, D) + _param_specs(params, H), dev)
+        _check_ws(ws, dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages),
                                               _ptr(block_table), _ptr(cache_lens), _ptr(o),
@@ -349,18 +389,20 @@ def bam_attn_decode_paged(q, k_pages, v_pages, block_table, cache_lens, o, lse,
     _check(st, "bam_attn_decode_paged")
 
 
-def bam_attn_decode_noalloc(q, kc, vc, o, lse, params: BamParams, stream=None) -> None:
+def bam_attn_decode_noalloc(q, kc, vc, o, lse, params: BamParams, stream=None,
+                            check=True) -> None:
     """Decode for callers that cannot allocate device memory (plugin-style
     hosts that only pass input/output pointers; loops that cannot afford
     cudaMalloc's possible synchronisation): no workspace argument, scratch
     from the library's fixed device array.  Overlapping calls race."""
     import torch
-    dev = _device(q)
     B, H, Tkv, D = kc.shape
-    for name, t in (("kc", kc), ("vc", vc)):
-        _require(t, name, (B, H, Tkv, D), (torch.bfloat16,), dev)
-    _check_decode_qo(q, o, lse, B, H, D, dev)
-    _check_params(params, H, dev)
+    if check:
+        dev = _device(q)
+        bf = _dt()[0]
+        kv = (B, H, Tkv, D)
+        _check_tensors((("kc", kc, kv, bf, False), ("vc", vc, kv, bf, False))
+                       + _decode_specs(q, o, lse, B, H, D) + _param_specs(params, H), dev)
     o_fp32 = 1 if o.dtype == torch.float32 else 0
     st = load_library().bam_attn_decode_noalloc(_ptr(q), _ptr(kc), _ptr(vc), _ptr(o), o_fp32,
                                                 _ptr(lse), B, H, Tkv, D, ctypes.byref(params),
