@@ -441,9 +441,11 @@ def run_ours(args, rank, world, dev, torch, dist):
     return line, t
 
 
-def extra_workloads(torch, dev, steps, peaks):
-    """Long-context prefill (causal, and the 32k one non-causal too) and decode
-    (parity configurations), timed briefly."""
+def extra_workloads(torch, dev, steps, peaks, cpu=True):
+    """The other workloads of the method, timed briefly: the small forward
+    (workload 1), the long-context prefills (causal, and the 32k one
+    non-causal too) and decode.  With `cpu`, each entry also carries the fp64
+    oracle's rate on the same inputs (in full, or on a stated sample)."""
     from transformer_attention_ggd_gb300 import bam_attn as ba
     from transformer_attention_ggd_gb300.inputs import make_inputs
 
@@ -452,13 +454,14 @@ def extra_workloads(torch, dev, steps, peaks):
     def bf(b):
         return torch.from_numpy(b.view(np.int16)).to(dev).view(torch.bfloat16)
 
-    for cfg, reps, causal in ((3, max(3, steps // 4), True), (4, 2, True),
-                              (3, max(3, steps // 4), False)):
+    for cfg, reps, causal in ((1, max(5, steps), True), (3, max(3, steps // 4), True),
+                              (4, 3, True), (3, max(3, steps // 4), False)):
         d = make_inputs(cfg)
         q, k, v = bf(d["q"]), bf(d["k"]), bf(d["v"])
         p = {n: torch.from_numpy(d[n]).to(dev) for n in ("alpha", "beta", "mu", "s")}
         B, H, T = d["B"], d["H"], d["T"]
-        prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, causal, True)
+        ssmax = bool(d["ssmax"])
+        prm = ba.make_params(p["alpha"], p["beta"], p["mu"], p["s"], 1e-5, causal, ssmax)
         o = torch.empty((B, H, T, D), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
         ws = ba.workspace(ba.BAM_OP_FWD, B, H, T, dev)
@@ -479,7 +482,8 @@ def extra_workloads(torch, dev, steps, peaks):
         fl = (pairs_causal(B, H, T) if causal else B * H * T * T) * 4 * D
         tf = fl / (statistics.median(ms) * 1e-3) / 1e12
         ktf = fl / (statistics.median(kms) * 1e-3) / 1e12
-        name = f"prefill_{'' if causal else 'noncausal_'}B{B}_H{H}_T{T}"
+        kind = "fwd" if cfg == 1 else "prefill"
+        name = f"{kind}_{'' if causal else 'noncausal_'}B{B}_H{H}_T{T}"
         out[name] = {
             "ms": round(statistics.median(ms), 4), "TFLOP/s": round(tf, 2),
             "fwd_kernel_TFLOP/s": round(ktf, 2),
@@ -487,6 +491,9 @@ def extra_workloads(torch, dev, steps, peaks):
             "traffic": traffic_for("bam_fwd_kernel", name)}
         del q, k, v, o, ws
         torch.cuda.empty_cache()
+        if cpu:
+            out[name]["cpu_baseline"] = (oracle_fwd_full(d, causal) if cfg == 1
+                                         else oracle_fwd_sampled(d, causal))
 
     d = make_inputs(5)
     q, kc, vc = bf(d["q"]), bf(d["k"]), bf(d["v"])
@@ -518,6 +525,8 @@ def extra_workloads(torch, dev, steps, peaks):
         "ms": round(statistics.median(ms), 4), "GB/s": round(gbs, 1),
         "decode_kernel_GB/s": round(kgbs, 1), "frac_of_hbm": round(kgbs / peaks["hbm_gbs"], 4),
         "traffic": traffic_for("bam_decode_kernel", name)}
+    if cpu:
+        out[name]["cpu_baseline"] = oracle_decode_full(d)
 
     # Ragged decode on the same cache: seeded lengths U[1, Tkv] per sequence;
     # the bytes are those of the keys each sequence actually holds.
@@ -589,6 +598,96 @@ def extra_workloads(torch, dev, steps, peaks):
 
 
 # ---------------------------------------------------------------- oracle arm
+
+def _oracle_entry(value, unit, seconds, sample, extra=None):
+    e = {"value": round(value, 6), "unit": unit, "cores": os.cpu_count() or 1, "kind": "oracle",
+         "seconds": round(seconds, 3), "sample": sample}
+    if extra:
+        e.update(extra)
+    return e
+
+
+def oracle_fwd_full(d, causal):
+    """The fp64 oracle's forward over a whole (small) workload."""
+    import oracle
+    from transformer_attention_ggd_gb300.inputs import bf16_to_f64
+    oracle.build()
+    B, H, T = d["B"], d["H"], d["T"]
+    x = {n: bf16_to_f64(d[n]) for n in ("q", "k", "v")}
+    t0 = time.perf_counter()
+    oracle.fwd(x["q"], x["k"], x["v"], d["alpha"], d["beta"], d["mu"], d["s"], causal=causal,
+               ssmax=bool(d["ssmax"]), nthreads=os.cpu_count() or 1)
+    dt = time.perf_counter() - t0
+    fl = (pairs_causal(B, H, T) if causal else B * H * T * T) * 4 * D
+    return _oracle_entry(fl / dt / 1e12, "TFLOP/s", dt,
+                         f"fp64 oracle forward of the whole workload (B={B} H={H} T={T})")
+
+
+def oracle_sample_rows(T, nrows, seed):
+    """Stratified query rows of a length-T sequence: one row drawn from each
+    of nrows equal strata, with rows 0 and T-1 always included."""
+    rng = np.random.default_rng(seed)
+    edges = np.linspace(0, T, nrows + 1).astype(np.int64)
+    rows = np.array([rng.integers(a, max(a + 1, b)) for a, b in zip(edges[:-1], edges[1:])])
+    rows[0], rows[-1] = 0, T - 1
+    return np.unique(rows)
+
+
+def oracle_fwd_sampled(d, causal, nrows=256, seed=7):
+    """The fp64 oracle's forward on a stratified sample of query rows of a
+    long-context prefill, dealt round-robin over the heads of batch row 0;
+    the rate is the sample's algorithmic flops (4 D per visible key) over the
+    oracle's time, and the full workload's time is extrapolated by the same
+    per-key cost (a causal row i costs i+1 keys)."""
+    import oracle
+    from transformer_attention_ggd_gb300.inputs import bf16_to_f64
+    oracle.build()
+    B, H, T = d["B"], d["H"], d["T"]
+    rows = oracle_sample_rows(T, nrows, seed)
+    dt, keys = 0.0, 0
+    for h in range(H):
+        mine = rows[h::H]
+        if mine.size == 0:
+            continue
+        x = {n: bf16_to_f64(d[n][0:1, h:h + 1]) for n in ("q", "k", "v")}
+        sel = {n: d[n][h:h + 1] for n in ("alpha", "beta", "mu", "s")}
+        t0 = time.perf_counter()
+        oracle.fwd_rows(x["q"], x["k"], x["v"], mine, sel["alpha"], sel["beta"], sel["mu"],
+                        sel["s"], causal=causal, ssmax=bool(d["ssmax"]),
+                        nthreads=os.cpu_count() or 1)
+        dt += time.perf_counter() - t0
+        keys += int((mine + 1).sum()) if causal else mine.size * T
+        del x
+    fl = keys * 4 * D
+    full_keys = (pairs_causal(B, H, T) if causal else B * H * T * T)
+    return _oracle_entry(fl / dt / 1e12, "TFLOP/s", dt,
+                         f"fp64 oracle forward of {rows.size} stratified query rows (rows 0 and "
+                         f"T-1 included) dealt over the {H} heads of batch row 0, "
+                         f"extrapolated by keys seen per row",
+                         {"extrapolated_full_s": round(full_keys / keys * dt, 1)})
+
+
+def oracle_decode_full(d):
+    """The fp64 oracle's decode over the whole cache, one batch row per call
+    (only the oracle calls are timed); the rate is in GB/s of the bf16 K and
+    V cache, as the kernel's."""
+    import oracle
+    from transformer_attention_ggd_gb300.inputs import bf16_to_f64
+    oracle.build()
+    B, H, Tkv = d["B"], d["H"], d["T"]
+    dt = 0.0
+    for b in range(B):
+        x = {n: bf16_to_f64(d[n][b:b + 1]) for n in ("q", "k", "v")}
+        t0 = time.perf_counter()
+        oracle.decode(x["q"], x["k"], x["v"], d["alpha"], d["beta"], d["mu"], d["s"],
+                      ssmax=bool(d["ssmax"]), nthreads=os.cpu_count() or 1)
+        dt += time.perf_counter() - t0
+        del x
+    kv_bytes = 2 * B * H * Tkv * D * 2
+    return _oracle_entry(kv_bytes / dt / 1e9, "GB/s", dt,
+                         f"fp64 oracle decode of all {B * H} (b,h) caches (B={B} H={H} "
+                         f"Tkv={Tkv}), one batch row per call")
+
 
 def oracle_sample_step(d, nbh, nthreads):
     """fwd + bwd of the fp64 oracle on the first `nbh` (b, h) pairs of the
@@ -776,7 +875,7 @@ def main():
         peaks = load_peaks()
         if not args.no_extra:
             _nvtx(torch, "prefill and decode extras")
-            line["extra"] = extra_workloads(torch, dev, args.steps, peaks)
+            line["extra"] = extra_workloads(torch, dev, args.steps, peaks, cpu=not args.no_cpu)
             _nvtx(torch, None)
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(seed=args.seed)

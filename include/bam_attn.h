@@ -40,7 +40,9 @@
  *    before anything is launched; launch failures return BAM_ERR_CUDA.
  *  - Every on-device wait is bounded.  A kernel that gives up records
  *    BAM_ERR_TIMEOUT in the workspace status word and returns; read it with
- *    bam_attn_check_status().
+ *    bam_attn_check_status().  A recorded error stays until it is read: a
+ *    later call on the same workspace runs normally but neither erases nor
+ *    overwrites it (the first error since the last check is reported).
  *  - One device per process (one process per GPU, as torch.distributed
  *    launches ranks): the kernels' shared-memory limits are raised once, on
  *    the device current at the first call.  On another device of the same
@@ -102,8 +104,10 @@ size_t bam_attn_workspace_size(int op, int B, int H, int T, int D);
 /* Forward (prefill).  q, k, v: bf16 [B,H,T,D].  o: [B,H,T,D], fp32 when
  * o_fp32 != 0, else bf16.  lse: fp32 [B,H,T] natural-log log-sum-exp of the
  * logits of each row (may be NULL; bam_attn_bwd needs it).  T >= 1.
- * Steps: per-head distance table b_h(d) (fp64 math, fp32 store) into ws, then
- * the fused tiled kernel (tensor-core QK^T and PV, online softmax). */
+ * Steps: per-head distance table b_h(d) into ws (fp32, with the exponent
+ * beta * log2(u / alpha) carried as a two-float sum so that b keeps a few
+ * 1e-7 relative error at any magnitude), then the fused tiled kernel
+ * (tensor-core QK^T and PV, online softmax). */
 bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, int o_fp32,
                         float* lse, int B, int H, int T, int D, const bam_params* p,
                         void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -124,7 +128,9 @@ bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void*
  * its key and value.  q: bf16 [B,H,D]; kc, vc: bf16 [B,H,Tkv,D].  The query
  * sits at position Tkv-1, every cached key is visible and n = Tkv.
  * o: [B,H,D] fp32 when o_fp32 != 0, else bf16; lse: fp32 [B,H] or NULL.
- * p->causal is ignored.  Split-KV partials go to ws. */
+ * p->causal is ignored.  Split-KV partials go to ws.  If a device wait of the
+ * call gives up, o and lse are written as NaN (and bam_attn_check_status
+ * reports BAM_ERR_TIMEOUT). */
 bam_status bam_attn_decode(const void* q, const void* kc, const void* vc, void* o, int o_fp32,
                            float* lse, int B, int H, int Tkv, int D, const bam_params* p,
                            void* ws, size_t ws_bytes, cudaStream_t stream);
@@ -163,8 +169,20 @@ bam_status bam_attn_decode_paged(const void* q, const void* k_pages, const void*
  * BAM_ERR_INVALID_ARG (a device-read argument was out of range: a ragged or
  * paged decode's cache length or page number), BAM_ERR_BOUNDS (debug build:
  * a bulk copy failed its bounds check and was not issued; the call's outputs
- * are then invalid) or BAM_ERR_CUDA. */
+ * are then invalid) or BAM_ERR_CUDA.  The result is the first error recorded
+ * by any call on `ws` since the previous check (errors are not cleared by
+ * later calls).  A workspace no call has used reports BAM_OK. */
 bam_status bam_attn_check_status(void* ws, cudaStream_t stream);
+
+/* Debug build only (bam_attn_debug_build() == 1; BAM_ERR_UNSUPPORTED
+ * otherwise): arms the give-up count of `ws`.  The next calls on `ws` count
+ * their bounded device waits, and the n-th one gives up as if its time limit
+ * had passed: the kernel records BAM_ERR_TIMEOUT, drains its own in-flight
+ * copies and tensor-core work, frees its Tensor Memory and returns, and the
+ * rest of the call follows the abort.  This drives the give-up paths of the
+ * real kernels without a hang.  n = 0 disarms.  Synchronises the device.
+ * Not part of any attention call. */
+bam_status bam_attn_debug_arm_giveup(void* ws, int n);
 
 /* 1 when the library was built with BAM_DEBUG, else 0.  The debug build is
  * the same library with every plain bulk copy (the distance-table windows of
@@ -203,12 +221,23 @@ const char* bam_status_string(bam_status s);
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture on the device.  All calls share the array:
  * calls that overlap on the GPU (for example on two streams) race on it.
- * A device-side give-up of this path is recorded in that array and is not
- * reported to the caller. */
+ * A device-side give-up writes NaN to o and lse and is recorded in that
+ * array; bam_attn_decode_noalloc_check_status reads it. */
 #define BAM_DECODE_NOALLOC_SCRATCH_BYTES (4u << 20)
 bam_status bam_attn_decode_noalloc(const void* q, const void* kc, const void* vc, void* o,
                                    int o_fp32, float* lse, int B, int H, int Tkv, int D,
                                    const bam_params* p, cudaStream_t stream);
+
+/* bam_attn_check_status for bam_attn_decode_noalloc on the current device:
+ * synchronises `stream`, then reads and clears the status words kept at the
+ * start of the no-alloc scratch array (the first error of any no-alloc call
+ * on this device since the previous check).  Allocates nothing.  The pages
+ * have no counterpart. */
+bam_status bam_attn_decode_noalloc_check_status(cudaStream_t stream);
+
+/* bam_attn_debug_arm_giveup for the no-alloc scratch of the current device
+ * (debug build only; BAM_ERR_UNSUPPORTED otherwise). */
+bam_status bam_attn_debug_arm_giveup_noalloc(int n);
 
 /* Kernels that bam_attn_profile_events can bracket. */
 enum {

@@ -56,6 +56,30 @@ def test_small_ragged(T, causal, ssmax):
     np.testing.assert_allclose(lse, lref, rtol=LSE_RTOL, atol=LSE_ATOL)
 
 
+@pytest.mark.parametrize("T", [129, 300, 513])
+@pytest.mark.parametrize("causal", [True, False])
+def test_paired_and_single_tile_schedules(T, causal):
+    """The forward runs 256-row CTAs (two query tiles sharing each K/V tile)
+    when they fill at least two waves of the SMs, else single-tile CTAs (128
+    rows, two per SM).  One (b, h) pair of heads runs the single-tile kernel;
+    the same heads repeated over 160 batch rows run paired; both match the
+    oracle, every repeat alike."""
+    rng = np.random.default_rng(T + 11 * causal)
+    H = 2
+    bits = {n: normal_bits(rng, (1, H, T, 64)) for n in "qkv"}
+    prm = random_params(H, rng, mu_hi=6.0)
+    prm["beta"][0] = -0.6
+    oref, lref = _oracle(bits, prm, causal, True)
+    o1, l1 = _run(bits, prm, causal, True)
+    np.testing.assert_allclose(o1, oref, rtol=0, atol=O_ATOL)
+    np.testing.assert_allclose(l1, lref, rtol=LSE_RTOL, atol=LSE_ATOL)
+    rep = {n: np.ascontiguousarray(np.repeat(b, 160, axis=0)) for n, b in bits.items()}
+    o2, l2 = _run(rep, prm, causal, True)
+    np.testing.assert_allclose(o2, np.repeat(oref, 160, axis=0), rtol=0, atol=O_ATOL)
+    np.testing.assert_allclose(l2, np.repeat(lref, 160, axis=0), rtol=LSE_RTOL, atol=LSE_ATOL)
+    assert (o2 == o2[:1]).all() and (l2 == l2[:1]).all()
+
+
 def test_worked_example_on_gpu():
     """Non-causal T=2, four heads, zero content, values 0 and 1 in column 0:
     head 0 gives 0.4378235, 0.5621765 (the ALiBi-style exercise's printed

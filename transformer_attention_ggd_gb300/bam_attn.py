@@ -63,8 +63,11 @@ EXPORTED = (
     "bam_attn_profile_events",
     "bam_attn_launch_count",
     "bam_attn_decode_noalloc",
+    "bam_attn_decode_noalloc_check_status",
     "bam_attn_selftest_wait",
     "bam_attn_debug_build",
+    "bam_attn_debug_arm_giveup",
+    "bam_attn_debug_arm_giveup_noalloc",
 )
 
 # Size of the fixed device scratch of bam_attn_decode_noalloc.
@@ -135,6 +138,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bam_attn_selftest_wait.argtypes = [vp, sz, vp]
         lib.bam_attn_debug_build.restype = i
         lib.bam_attn_debug_build.argtypes = []
+        lib.bam_attn_decode_noalloc_check_status.restype = i
+        lib.bam_attn_decode_noalloc_check_status.argtypes = [vp]
+        lib.bam_attn_debug_arm_giveup.restype = i
+        lib.bam_attn_debug_arm_giveup.argtypes = [vp, i]
+        lib.bam_attn_debug_arm_giveup_noalloc.restype = i
+        lib.bam_attn_debug_arm_giveup_noalloc.argtypes = [i]
         _lib = lib
         return lib
 
@@ -421,9 +430,27 @@ def bam_attn_check_status(ws, stream=None) -> int:
     return int(load_library().bam_attn_check_status(_ptr(ws), _stream(stream)))
 
 
+def bam_attn_decode_noalloc_check_status(stream=None) -> int:
+    """Status of the no-alloc decode calls on the current device since the
+    previous check (synchronises the stream; reads and clears)."""
+    return int(load_library().bam_attn_decode_noalloc_check_status(_stream(stream)))
+
+
 def bam_attn_debug_build() -> bool:
     """True when the loaded library is the bounds-checking debug build."""
     return bool(load_library().bam_attn_debug_build())
+
+
+def bam_attn_debug_arm_giveup(ws, n: int) -> int:
+    """Debug build: the n-th bounded device wait of the next calls on `ws`
+    gives up (0 disarms).  Returns the status (BAM_ERR_UNSUPPORTED in the
+    release build)."""
+    return int(load_library().bam_attn_debug_arm_giveup(_ptr(ws), int(n)))
+
+
+def bam_attn_debug_arm_giveup_noalloc(n: int) -> int:
+    """As bam_attn_debug_arm_giveup, for the no-alloc decode's scratch."""
+    return int(load_library().bam_attn_debug_arm_giveup_noalloc(int(n)))
 
 
 def bam_attn_profile_events(which: int, before=None, after=None) -> None:

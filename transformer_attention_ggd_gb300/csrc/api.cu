@@ -247,6 +247,65 @@ bam_status decode_impl(const void* q, const void* kc, const void* vc, const int*
 }
 
 }  // namespace
+
+// For bam_attn_decode_noalloc (decode_noalloc.cu): the argument checks, the
+// scratch size and the launches of bam_attn_decode, on caller-given scratch.
+bam_status decode_args_ok(const void* q, const void* kc, const void* vc, void* o, float* lse,
+                          int B, int H, int Tkv, int D, const bam_params* p) {
+  bam_status s = check_sizes(B, H, Tkv, D);
+  if (s != BAM_OK) return s;
+  if ((s = check_params(p)) != BAM_OK) return s;
+  if (!q || !kc || !vc || !o) return BAM_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kc, 16) || !aligned(vc, 16) || !aligned(o, 16) ||
+      (lse && !aligned(lse, 4)))
+    return BAM_ERR_INVALID_ARG;
+  return BAM_OK;
+}
+size_t decode_scratch_bytes(int B, int H, int Tkv) { return dec_ws(B, H, Tkv).total; }
+bam_status decode_plain(const void* q, const void* kc, const void* vc, void* o, int o_fp32,
+                        float* lse, int B, int H, int Tkv, int D, const bam_params* p,
+                        void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  return decode_impl(q, kc, vc, nullptr, o, o_fp32, lse, B, H, Tkv, D, p, scratch, scratch_bytes,
+                     stream);
+}
+// Reads and clears the status words at `st` (device memory) after
+// synchronising `stream`; the sticky-error rules of bam_attn_check_status.
+bam_status read_and_clear_status(void* st_dev, cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return BAM_ERR_CUDA;
+  DevStatus st;
+  if (cudaMemcpy(&st, st_dev, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BAM_ERR_CUDA;
+  // A status area no call has initialised holds no error.
+  if (st.magic[0] != kStatusMagic0 || st.magic[1] != kStatusMagic1) return BAM_OK;
+  // Clears abort, code, site and block; the magic and the debug count stay.
+  if (cudaMemset(st_dev, 0, 4 * sizeof(int)) != cudaSuccess) return BAM_ERR_CUDA;
+  if (st.code == BAM_DEV_BAD_ARG && st.abort == 0) return BAM_ERR_INVALID_ARG;
+  if (st.code == BAM_DEV_BOUNDS) return BAM_ERR_BOUNDS;
+  if (st.code != BAM_DEV_OK || st.abort != 0) return BAM_ERR_TIMEOUT;
+  return BAM_OK;
+}
+// Debug builds: arms the give-up count of the status words at `st_dev`.
+bam_status arm_giveup(void* st_dev, int n) {
+#ifdef BAM_DEBUG
+  DevStatus st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return BAM_ERR_CUDA;
+  if (cudaMemcpy(&st, st_dev, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BAM_ERR_CUDA;
+  if (st.magic[0] != kStatusMagic0 || st.magic[1] != kStatusMagic1) {
+    std::memset(&st, 0, sizeof(st));
+    st.magic[0] = kStatusMagic0;
+    st.magic[1] = kStatusMagic1;
+  }
+  st.giveup = n;
+  if (cudaMemcpy(st_dev, &st, sizeof(st), cudaMemcpyHostToDevice) != cudaSuccess)
+    return BAM_ERR_CUDA;
+  return BAM_OK;
+#else
+  (void)st_dev;
+  (void)n;
+  return BAM_ERR_UNSUPPORTED;
+#endif
+}
 }  // namespace bam
 
 using namespace bam;
@@ -303,7 +362,6 @@ bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, in
   fa.B = B;
   fa.H = H;
   fa.T = T;
-  fa.nqb = (T + 255) / 256;
   fa.causal = p->causal;
   fa.ssmax = p->ssmax;
   fa.o_fp32 = o_fp32 ? 1 : 0;
@@ -426,14 +484,13 @@ bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void*
 
 bam_status bam_attn_check_status(void* ws, cudaStream_t stream) {
   if (!ws || !aligned(ws, 256)) return BAM_ERR_WORKSPACE;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return BAM_ERR_CUDA;
-  DevStatus st;
-  if (cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return BAM_ERR_CUDA;
-  if (cudaMemset(ws, 0, sizeof(st)) != cudaSuccess) return BAM_ERR_CUDA;
-  if (st.code == BAM_DEV_BAD_ARG && st.abort == 0) return BAM_ERR_INVALID_ARG;
-  if (st.code == BAM_DEV_BOUNDS) return BAM_ERR_BOUNDS;
-  if (st.code != BAM_DEV_OK || st.abort != 0) return BAM_ERR_TIMEOUT;
-  return BAM_OK;
+  return read_and_clear_status(ws, stream);
+}
+
+bam_status bam_attn_debug_arm_giveup(void* ws, int n) {
+  if (n < 0) return BAM_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return BAM_ERR_WORKSPACE;
+  return arm_giveup(ws, n);
 }
 
 int bam_attn_debug_build(void) {

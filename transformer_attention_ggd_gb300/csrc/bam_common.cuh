@@ -73,7 +73,7 @@ struct TableArgs {
   const float* alpha;
   const float* beta;
   const float* mu;
-  DevStatus* status;  // zeroed by block 0 (the first kernel of every call)
+  DevStatus* status;  // the call's status words (status_begin_call in block 0)
   float eps;
   int H, len, off, Tkv, mode;
   int prior;  // BAM_PRIOR_ALPHA or BAM_PRIOR_THETA (alpha, beta, mu hold the thetas)
@@ -85,7 +85,7 @@ struct FwdArgs {
   const float* table;
   const float* s;
   DevStatus* status;
-  int B, H, T, nqb;
+  int B, H, T;
   int causal, ssmax, o_fp32;
   int tab_len, tab_off;
 };

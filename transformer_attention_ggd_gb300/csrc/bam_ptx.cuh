@@ -89,13 +89,40 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
-// Device status words shared by every CTA of a launch (in the caller's workspace).
+// Device status words shared by every CTA of a launch (in the caller's
+// workspace).  The first error recorded stays until the host reads it
+// (bam_attn_check_status): the first kernel of each call clears only the
+// abort word, so that a later call on the same workspace neither erases nor
+// overwrites an unread error.  `magic` marks a status area that has been
+// initialised; a workspace whose magic does not match (fresh memory) has
+// its status cleared by the first kernel of the call instead.
 struct DevStatus {
   int abort;      // nonzero: some thread gave up; everyone else leaves early
   int code;       // first error code recorded (BAM_DEV_*)
   int site;       // where it happened (kernel-specific)
   int block;      // which block
+  unsigned magic[2];
+  // Debug builds (BAM_DEBUG) only: when positive, the bounded waits of the
+  // call count it down and the wait that takes it to zero gives up as if its
+  // time limit had passed (bam_attn_debug_arm_giveup).  Ignored otherwise.
+  int giveup;
 };
+
+constexpr unsigned kStatusMagic0 = 0x4d414221u, kStatusMagic1 = 0x53544154u;
+
+// Start of a call: one thread of the call's first kernel, before any other
+// kernel of the call looks at the status.
+__device__ __forceinline__ void status_begin_call(DevStatus* st) {
+  if (st->magic[0] != kStatusMagic0 || st->magic[1] != kStatusMagic1) {
+    st->code = 0;
+    st->site = 0;
+    st->block = 0;
+    st->giveup = 0;
+    st->magic[0] = kStatusMagic0;
+    st->magic[1] = kStatusMagic1;
+  }
+  st->abort = 0;
+}
 
 // BAM_DEV_BAD_ARG: an argument only the device reads was out of range (a
 // cache length of the ragged decode); the kernel clamped it and went on.
@@ -151,9 +178,18 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 }
 
 // Bounded wait on phase `parity`.  Returns false when the wait gave up (own
-// timeout, a CTA-local abort, or the grid-wide abort word).
+// timeout, a CTA-local abort, or the grid-wide abort word).  In a debug build
+// an armed give-up count (DevStatus::giveup) makes the wait that exhausts it
+// give up at once, as if its time limit had passed, so that tests can drive
+// every kernel through its give-up and drain path.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, DevStatus* st,
                                           volatile int* cta_abort, int site) {
+#ifdef BAM_DEBUG
+  if (*reinterpret_cast<volatile int*>(&st->giveup) > 0 && atomicSub(&st->giveup, 1) == 1) {
+    raise_abort(st, cta_abort, site);
+    return false;
+  }
+#endif
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, st, cta_abort, site);
 }

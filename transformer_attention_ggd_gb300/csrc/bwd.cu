@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
 __global__ void __launch_bounds__(256) bam_bwd_prep_kernel(const BwdArgs a, int table_blocks) {
   grid_dep_trigger();
   if (static_cast<int>(blockIdx.x) < table_blocks) {
-    if (blockIdx.x == 0 && threadIdx.x < 4) reinterpret_cast<int*>(a.status)[threadIdx.x] = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) status_begin_call(a.status);  // the call starts here
     const size_t n = static_cast<size_t>(a.tab.H) * a.tab.len;
     for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
          e += static_cast<size_t>(table_blocks) * blockDim.x)

@@ -280,7 +280,19 @@ __global__ void __launch_bounds__(128) bam_decode_combine_kernel(const DecodeArg
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x * 4 + warp;
   if (bh >= a.B * a.H) return;
-  if (*reinterpret_cast<volatile int*>(&a.status->abort)) return;
+  const size_t off = static_cast<size_t>(bh) * kHeadDim + 2 * lane;
+  if (*reinterpret_cast<volatile int*>(&a.status->abort)) {
+    // The call gave up: its partials are incomplete, so the outputs are
+    // marked invalid (NaN) rather than left as they were.
+    const float nan = __int_as_float(0x7fc00000);
+    if (a.o_fp32) {
+      reinterpret_cast<float2*>(static_cast<float*>(a.o) + off)[0] = make_float2(nan, nan);
+    } else {
+      reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.o) + off)[0] = 0x7fc07fc0u;
+    }
+    if (a.lse && lane == 0) a.lse[bh] = nan;
+    return;
+  }
   const float* part = a.part + static_cast<size_t>(bh) * a.nsplit * kPartStride;
   float M = -INFINITY;
   for (int sp = 0; sp < a.nsplit; ++sp) M = fmaxf(M, part[sp * kPartStride]);
@@ -293,7 +305,6 @@ __global__ void __launch_bounds__(128) bam_decode_combine_kernel(const DecodeArg
     o1 += p[3 + 2 * lane] * sc;
   }
   const float inv = 1.0f / L;
-  const size_t off = static_cast<size_t>(bh) * kHeadDim + 2 * lane;
   if (a.o_fp32) {
     reinterpret_cast<float2*>(static_cast<float*>(a.o) + off)[0] = make_float2(o0 * inv, o1 * inv);
   } else {

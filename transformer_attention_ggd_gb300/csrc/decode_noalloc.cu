@@ -16,9 +16,14 @@
 // the first call on each device does this set-up (make that first call
 // before any stream capture on the device).  All calls share the array and it
 // keeps the last call's contents: the table and every partial are fully
-// rewritten by each call and the status word is cleared by the table kernel,
-// so nothing else has to start at zero; calls that overlap on the GPU (for
-// example on two streams) race on it.
+// rewritten by each call, and the status words at its start follow the
+// workspace rules (the first kernel of a call clears the abort word; an
+// error stays until bam_attn_decode_noalloc_check_status reads it), so
+// nothing has to start at zero; calls that overlap on the GPU (for example on
+// two streams) race on it.
+//
+// Argument checks, scratch layout and launches are those of bam_attn_decode
+// (api.cu), on the array instead of a workspace.
 #include <mutex>
 
 #include "../../include/bam_attn.h"
@@ -26,8 +31,15 @@
 
 namespace bam {
 
-// Launch counter of the library (defined with the other entry points).
-void note_launches(int n);
+// The decode path of bam_attn_decode (api.cu).
+bam_status decode_args_ok(const void* q, const void* kc, const void* vc, void* o, float* lse,
+                          int B, int H, int Tkv, int D, const bam_params* p);
+size_t decode_scratch_bytes(int B, int H, int Tkv);
+bam_status decode_plain(const void* q, const void* kc, const void* vc, void* o, int o_fp32,
+                        float* lse, int B, int H, int Tkv, int D, const bam_params* p,
+                        void* scratch, size_t scratch_bytes, cudaStream_t stream);
+bam_status read_and_clear_status(void* st_dev, cudaStream_t stream);
+bam_status arm_giveup(void* st_dev, int n);
 
 namespace {
 
@@ -58,8 +70,6 @@ cudaError_t scratch_for_current_device(void** out) {
   return cudaSuccess;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-
 }  // namespace
 }  // namespace bam
 
@@ -69,67 +79,25 @@ extern "C" bam_status bam_attn_decode_noalloc(const void* q, const void* kc, con
                                               void* o, int o_fp32, float* lse, int B, int H,
                                               int Tkv, int D, const bam_params* p,
                                               cudaStream_t stream) {
-  if (B < 1 || H < 1 || Tkv < 1 || D < 1) return BAM_ERR_INVALID_ARG;
-  if (D != kHeadDim) return BAM_ERR_UNSUPPORTED;
-  if (Tkv > (1 << 28) || H > 65535 || static_cast<int64_t>(B) * H > (1 << 24))
-    return BAM_ERR_UNSUPPORTED;
-  if (!p || !p->alpha || !p->beta || !p->mu || (p->ssmax && !p->s)) return BAM_ERR_INVALID_ARG;
-  if (!(p->eps > 0.0f) || !(p->eps < 3.0e38f)) return BAM_ERR_INVALID_ARG;
-  if (p->ssmax != 0 && p->ssmax != 1) return BAM_ERR_INVALID_ARG;
-  if (p->prior != BAM_PRIOR_ALPHA && p->prior != BAM_PRIOR_THETA) return BAM_ERR_INVALID_ARG;
-  if (!q || !kc || !vc || !o) return BAM_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(o) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3) != 0))
-    return BAM_ERR_INVALID_ARG;
-
-  // Scratch layout (same as the workspace of bam_attn_decode): status words,
-  // the decode table, the split partials.
-  int nsplit = 0, chunk = 0;
-  decode_split(B * H, Tkv, &nsplit, &chunk);
-  const int tab_len = decode_table_len(Tkv);
-  const size_t table_off = kStatusBytes;
-  const size_t part_off = table_off + align256(static_cast<size_t>(H) * tab_len * 4);
-  const size_t need =
-      part_off + align256(static_cast<size_t>(B) * H * nsplit * (2 + kHeadDim) * 4);
-  if (need > kNoAllocScratchBytes) return BAM_ERR_WORKSPACE;
-
+  // Every refusal comes before the array's address is looked up.
+  bam_status s = decode_args_ok(q, kc, vc, o, lse, B, H, Tkv, D, p);
+  if (s != BAM_OK) return s;
+  if (decode_scratch_bytes(B, H, Tkv) > kNoAllocScratchBytes) return BAM_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return BAM_ERR_CUDA;
-  uint8_t* wsb = static_cast<uint8_t*>(scratch);
-  DevStatus* status = reinterpret_cast<DevStatus*>(wsb);
-  float* table = reinterpret_cast<float*>(wsb + table_off);
+  return decode_plain(q, kc, vc, o, o_fp32, lse, B, H, Tkv, D, p, scratch, kNoAllocScratchBytes,
+                      stream);
+}
 
-  TableArgs ta{table, p->alpha, p->beta, p->mu, status, p->eps, H, tab_len, 0, Tkv,
-               kTableDecode, p->prior};
-  cudaError_t e = launch_table(ta, stream);
-  note_launches(1);
-  if (e != cudaSuccess) return BAM_ERR_CUDA;
+extern "C" bam_status bam_attn_decode_noalloc_check_status(cudaStream_t stream) {
+  void* scratch = nullptr;
+  if (scratch_for_current_device(&scratch) != cudaSuccess) return BAM_ERR_CUDA;
+  return read_and_clear_status(scratch, stream);
+}
 
-  DecodeArgs da;
-  da.q = static_cast<const uint16_t*>(q);
-  da.kc = static_cast<const uint16_t*>(kc);
-  da.vc = static_cast<const uint16_t*>(vc);
-  da.lens = nullptr;
-  da.block_table = nullptr;
-  da.page = da.max_blocks = da.num_pages = 0;
-  da.table = table;
-  da.s = p->s;
-  da.part = reinterpret_cast<float*>(wsb + part_off);
-  da.o = o;
-  da.lse = lse;
-  da.status = status;
-  da.B = B;
-  da.H = H;
-  da.Tkv = Tkv;
-  da.nsplit = nsplit;
-  da.chunk = chunk;
-  da.tab_len = tab_len;
-  da.ssmax = p->ssmax;
-  da.o_fp32 = o_fp32 ? 1 : 0;
-  e = launch_decode(da, stream);
-  note_launches(1);
-  if (e != cudaSuccess) return BAM_ERR_CUDA;
-  e = launch_decode_combine(da, stream);
-  note_launches(1);
-  return e == cudaSuccess ? BAM_OK : BAM_ERR_CUDA;
+extern "C" bam_status bam_attn_debug_arm_giveup_noalloc(int n) {
+  if (n < 0) return BAM_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  if (scratch_for_current_device(&scratch) != cudaSuccess) return BAM_ERR_CUDA;
+  return arm_giveup(scratch, n);
 }

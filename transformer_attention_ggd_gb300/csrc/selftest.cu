@@ -16,6 +16,7 @@ __global__ void bam_selftest_wait_kernel(DevStatus* st) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
+    status_begin_call(st);
     abort_flag = 0;
     mbar_init(&bar, 1);
     fence_barrier_init();

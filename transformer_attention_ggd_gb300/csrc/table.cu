@@ -24,9 +24,8 @@ namespace {
 __global__ void bam_table_kernel(const TableArgs a) {
   // Let the next kernel of this call start its prologue.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4) {
-    reinterpret_cast<int*>(a.status)[threadIdx.x] = 0;
-  }
+  // First kernel of every call that builds a table: the call starts here.
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) status_begin_call(a.status);
   const int h = blockIdx.y;
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
   if (h >= a.H || x >= a.len) return;
