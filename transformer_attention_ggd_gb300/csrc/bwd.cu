@@ -460,33 +460,39 @@ __global__ void __launch_bounds__(kBThreads, 1)
       return true;
     };
     int g = 0;
+    // The row data of a query tile (this thread's LSE and Delta) and the
+    // item's SSMax scale are loaded one tile ahead, across item boundaries
+    // too, so that no global load sits at the start of a tile.
+    float lse_nx = 0.f, del_nx = 0.f, s_nx = 1.0f;
+    auto prefetch_row = [&](int bh_, int i_, int h_) {
+      if (i_ < a.T) {
+        lse_nx = __ldg(a.lse + static_cast<size_t>(bh_) * a.T + i_);
+        del_nx = __ldg(a.delta + static_cast<size_t>(bh_) * a.T + i_);
+      }
+      if (h_ >= 0) s_nx = a.ssmax ? __ldg(a.s + h_) : 1.0f;
+    };
     BwdItem it;
-    for (int round = 0; ok && bwd_item(a, round, it); ++round) {
+    bool have = bwd_item(a, 0, it);
+    if (have) prefetch_row(it.bh, it.q_first * 128 + r, it.h);
+    for (int round = 0; ok && have; ++round) {
       const int bh = it.bh, j0 = it.j0, q_first = it.q_first, nq = it.nq;
-      const float s_h = a.ssmax ? __ldg(a.s + it.h) : 1.0f;
+      const float s_h = s_nx;
       // Scalar-gradient sums of the item as f32x2 pairs (even / odd key
       // columns): sum dS b (log2 units), sum dS db/dbeta, sum dS db/dmu, and
       // sum over rows of w_i * sum_j dS S.
       uint64_t accB2 = 0ull, accBeta2 = 0ull, accMu2 = 0ull;
       float acc_s = 0.f;
-      // LSE and Delta of this thread's row, one query tile ahead.
-      float lse_nx = 0.f, del_nx = 0.f;
-      {
-        const int i = q_first * 128 + r;
-        if (i < a.T) {
-          lse_nx = __ldg(a.lse + static_cast<size_t>(bh) * a.T + i);
-          del_nx = __ldg(a.delta + static_cast<size_t>(bh) * a.T + i);
-        }
-      }
       for (int t = 0; ok && t < nq; ++t, ++g) {
         const int s = g % kBStages;
         const int i0 = (q_first + t) * 128;
         const int i = i0 + r;
         const bool row_ok = i < a.T;
         const float lse_row = lse_nx, del_row = del_nx;
-        if (t + 1 < nq && i + 128 < a.T) {
-          lse_nx = __ldg(a.lse + static_cast<size_t>(bh) * a.T + i + 128);
-          del_nx = __ldg(a.delta + static_cast<size_t>(bh) * a.T + i + 128);
+        if (t + 1 < nq) {
+          prefetch_row(bh, i + 128, -1);
+        } else {
+          BwdItem nxt;
+          if (bwd_item(a, round + 1, nxt)) prefetch_row(nxt.bh, nxt.q_first * 128 + r, nxt.h);
         }
         // Per-row constants.
         const float n = a.causal ? static_cast<float>(i + 1) : static_cast<float>(a.T);
@@ -708,6 +714,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
           if (lane == 0) mbar_arrive(&sm.epi_full);
         }
       }
+      have = bwd_item(a, round + 1, it);
     }
     // A warp that gave up inside a tile may still have TMEM stores in
     // flight; they complete before the columns are freed.

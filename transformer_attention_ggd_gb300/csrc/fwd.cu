@@ -13,8 +13,8 @@
 // Long sequences (bam_fwd_kernel): one CTA owns 256 query rows of one (b, h)
 // as two 128-row tiles A and B, and both walk every key/value tile of 128
 // keys that they see, so each K/V tile loaded serves 256 rows.  Short
-// sequences use a single-tile form of the same pipeline, two CTAs per SM
-// (bam_fwd_single_kernel, below).
+// sequences use a persistent single-tile form of the same pipeline, two
+// CTAs per SM (bam_fwd_single_kernel, below).
 // Warp roles:
 //   warp 8      TMA producer: Q; per key tile K, V and the 384-entry
 //               distance window (four shifted reversed copies, so that a
@@ -130,29 +130,30 @@ __device__ __forceinline__ uint32_t fwd_setup(FwdSmem& sm, int warp) {
 // Issues the K, window and V copies of key tile j of head bh (query rows
 // from i0) into stage s, armed on k_full[s] and v_full[s].  `first` marks
 // the CTA's first tile: the windows come from the table kernel, which the
-// producer waits for there.  Returns false when a debug bounds check refused
-// a window copy.
-template <class Sm>
+// producer waits for there.  Windows hold W entries (384 for 256 query rows,
+// 256 for 128), each reversed copy W + 4, copies WS floats apart.  Returns
+// false when a debug bounds check refused a window copy.
+template <int W = kWin, int WS = kWinCopyStride, class Sm>
 __device__ __forceinline__ bool load_kv_tile(Sm& sm, const FwdArgs& a,
                                              const CUtensorMap* tk, const CUtensorMap* tv,
                                              int s, int j, int bh, int h, int i0, bool first,
                                              volatile int* ab) {
   // The window of key tile j covers table indices tab_off + i0 - 128 -
-  // 128 j + [0, kWin); in the reversed rows it starts at tab_len - kWin
-  // minus that base (a multiple of 4 entries).  A window starts inside its
-  // own row and may run past the row's end into the padding after the last
-  // row, never beyond it.
+  // 128 j + [0, W); in the reversed rows it starts at tab_len - W minus
+  // that base (a multiple of 4 entries).  A window starts inside its own row
+  // and may run past the row's end into the padding after the last row,
+  // never beyond it.
   const size_t copy_stride = static_cast<size_t>(a.H) * a.tab_len;
   const float* tab_h = a.table + static_cast<size_t>(h) * a.tab_len +
-                       (a.tab_len - kWin - a.tab_off - i0 + 128);
+                       (a.tab_len - W - a.tab_off - i0 + 128);
   const float* tab_end = a.table + kTabCopies * copy_stride + kTabPadFloats;
-  mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes + kTabCopies * kWinCopy * 4);
+  mbar_arrive_expect_tx(&sm.k_full[s], kTileBytes + kTabCopies * (W + 4) * 4);
   tma_load_3d(sm.k[s], tk, &sm.k_full[s], 0, 128 * j, bh);
   if (first) grid_dep_wait();
   bool ok = true;
   for (int k = 0; k < kTabCopies; ++k)
-    ok &= bulk_load_checked(sm.win[s] + win_copy_off(k, kWinCopyStride),
-                            tab_h + k * copy_stride + 128 * j, kWinCopy * 4, &sm.k_full[s],
+    ok &= bulk_load_checked(sm.win[s] + win_copy_off(k, WS),
+                            tab_h + k * copy_stride + 128 * j, (W + 4) * 4, &sm.k_full[s],
                             a.table + k * copy_stride + static_cast<size_t>(h) * a.tab_len,
                             tab_end, a.status, ab, kSiteWindowCopy);
   mbar_arrive_expect_tx(&sm.v_full[s], kTileBytes);
@@ -340,11 +341,13 @@ __device__ __forceinline__ bool softmax_tile(Sm& sm, SoftRow& row, int t, int s,
 // Columns [32 hb, 32 hb + 32) of row r of a finished tile (32 fp32 values
 // in ov), normalised, into the staging tile `ost` for its TMA store:
 // 128-byte rows with 16-byte chunk c at (c ^ (r % 8)) * 16; fp32 as two boxes
-// of 32 columns (box hb), bf16 as one box of 64 (chunks 4 hb .. 4 hb + 3).
+// of 32 columns (box hb at hb * box_stride), bf16 as one box of 64 (chunks
+// 4 hb .. 4 hb + 3).
 __device__ __forceinline__ void stage_half(const FwdArgs& a, uint8_t* ost, const uint32_t* ov,
-                                           int hb, float inv_l, int r) {
+                                           int hb, float inv_l, int r,
+                                           int box_stride = kTileBytes) {
   if (a.o_fp32) {
-    uint8_t* rowp = ost + hb * kTileBytes + r * 128;
+    uint8_t* rowp = ost + hb * box_stride + r * 128;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const uint32_t* v4 = ov + 4 * c;
@@ -580,22 +583,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ================================================================ single
-// Short sequences: one CTA per 128-row query tile, one softmax group, small
-// enough (256 TMEM columns, ~93 KB of shared memory) that two CTAs share an
-// SM.  Where paired CTAs would fill less than two waves of the SMs, this
-// doubles the CTAs and halves each one's footprint, and the hardware
-// overlaps one CTA's start (loads, first products) and end (O store) with
-// the other's softmax.  Two K/V stages; the finished O is staged in the K
-// stages, which the last PV product leaves free.
+// Short sequences: single-tile items (128 query rows of one (b, h)) on a
+// persistent grid of two CTAs per SM.  Where paired CTAs would fill less than
+// two waves of the SMs, a CTA per 256 rows leaves a ragged second wave of
+// short tiles at the end; here each CTA walks a list of items (longest first,
+// dealt in rounds of alternating direction, so that the short items of the
+// last round go to the CTAs whose first items were short), one softmax group
+// per CTA, 256 TMEM columns and ~107 KB of shared memory so that two CTAs
+// share an SM and overlap each other's loads, first products and O stores.
+// The K/V ring runs on across items; Q is reloaded once the item's last S
+// product has read it; O leaves through a 16 KB staging box (fp32 in two
+// passes of 32 columns).
 constexpr int kStages1 = 2;
 constexpr int kThreads1 = 192;  // softmax warps 0-3, producer 4, MMA issuer 5
+constexpr int kWin1 = 256;      // window entries per key tile (one query tile)
+constexpr int kWin1CopyStride = 288;
+constexpr int kWin1Stage = kTabCopies * kWin1CopyStride;
+static_assert(win_copy_off(kTabCopies - 1, kWin1CopyStride) + kWin1 + 4 <= kWin1Stage, "window");
 
 struct __align__(1024) Fwd1Smem {
   uint8_t q[1][kTileBytes];
-  uint8_t k[kStages1][kTileBytes];  // then the O staging tile (two 16 KB boxes)
+  uint8_t k[kStages1][kTileBytes];
   uint8_t v[kStages1][kTileBytes];
-  float win[kStages1][kWinStage];
+  uint8_t ost[kTileBytes];  // one 128-byte-swizzled box of O rows for a TMA store
+  float win[kStages1][kWin1Stage];
   uint64_t q_full[1];
+  uint64_t q_empty;   // the item's S products are done with its Q
   uint64_t k_full[kStages1];
   uint64_t v_full[kStages1];
   uint64_t kv_empty[kStages1];
@@ -603,12 +616,31 @@ struct __align__(1024) Fwd1Smem {
   uint64_t s_free[1];
   uint64_t p_full[1];
   uint64_t pv_done[1];
-  uint64_t o_full[1];
+  uint64_t o_full[1];  // the four softmax warps have staged a box
+  uint64_t ost_free;   // the staged box has been read by its TMA store
   uint64_t mma_final;
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(Fwd1Smem) + 1024 <= 113 * 1024, "two CTAs per SM");
+
+// Item n of this persistent CTA: query tile qt of head bh (nKV key tiles).
+struct Item1 {
+  int qt, bh, h, nKV;
+};
+
+__device__ __forceinline__ bool single_item(const FwdArgs& a, int n, Item1& it) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const int BH = a.B * a.H, nqt = (a.T + 127) / 128;
+  const int idx = n * G + ((n & 1) ? (G - 1 - c) : c);
+  if (idx >= nqt * BH) return false;
+  const int q = idx / BH;
+  it.qt = a.causal ? nqt - 1 - q : q;
+  it.bh = idx % BH;
+  it.h = it.bh % a.H;
+  it.nKV = a.causal ? it.qt + 1 : nqt;
+  return true;
+}
 
 // TMEM columns (256): S [0,128) P [128,192) O [192,256).
 __global__ void __launch_bounds__(kThreads1, 2)
@@ -620,21 +652,12 @@ __global__ void __launch_bounds__(kThreads1, 2)
   Fwd1Smem& sm = *reinterpret_cast<Fwd1Smem*>(smem_raw + ((0u - smem_u32(smem_raw)) & 1023u));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // Work item: causal query tiles with the most key tiles go first.
-  const int BH = a.B * a.H;
-  const int nqt = (a.T + 127) / 128;
-  const int qt = a.causal ? (nqt - 1 - static_cast<int>(blockIdx.x) / BH)
-                          : static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int h = bh % a.H;
-  const int i0 = qt * 128;
-  const int nKV = a.causal ? qt + 1 : nqt;
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
     sm.abort_flag = 0;
     mbar_init(&sm.q_full[0], 1);
+    mbar_init(&sm.q_empty, 1);
     for (int s = 0; s < kStages1; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
@@ -645,6 +668,7 @@ __global__ void __launch_bounds__(kThreads1, 2)
     mbar_init(&sm.p_full[0], 4);
     mbar_init(&sm.pv_done[0], 1);
     mbar_init(&sm.o_full[0], 4);
+    mbar_init(&sm.ost_free, 1);
     mbar_init(&sm.mma_final, 1);
     fence_barrier_init();
   }
@@ -660,65 +684,87 @@ __global__ void __launch_bounds__(kThreads1, 2)
   // kernel; everyone else waits here before looking at the status word.
   if (warp != 4) grid_dep_wait();
 
+  // Barrier phases run on over the CTA's items: Q by item, the K/V stages
+  // and the per-tile barriers by the running key-tile count.
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = (*ab == 0);
-      int issued = 0;
-      bool q_issued = false;
-      if (ok) {
-        prefetch_tmap(&tq);
-        prefetch_tmap(&tk);
-        prefetch_tmap(&tv);
-        mbar_arrive_expect_tx(&sm.q_full[0], kTileBytes);
-        tma_load_3d(sm.q[0], &tq, &sm.q_full[0], 0, i0, bh);
-        q_issued = true;
-      }
-      for (int j = 0; ok && j < nKV; ++j) {
-        const int s = j % kStages1;
-        if (j >= kStages1) {
-          ok = mbar_wait(&sm.kv_empty[s], ((j / kStages1) - 1) & 1, a.status, ab, kSiteProducer);
+      int jg = 0, q_items = 0;
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      Item1 it;
+      for (int n = 0; ok && single_item(a, n, it); ++n) {
+        if (n > 0) {
+          ok = mbar_wait(&sm.q_empty, (n - 1) & 1, a.status, ab, kSiteProducer);
           if (!ok) break;
         }
-        ok = load_kv_tile(sm, a, &tk, &tv, s, j, bh, h, i0, j == 0, ab);
-        issued = j + 1;
+        mbar_arrive_expect_tx(&sm.q_full[0], kTileBytes);
+        tma_load_3d(sm.q[0], &tq, &sm.q_full[0], 0, 128 * it.qt, it.bh);
+        q_items = n + 1;
+        for (int j = 0; ok && j < it.nKV; ++j, ++jg) {
+          const int s = jg % kStages1;
+          if (jg >= kStages1) {
+            ok = mbar_wait(&sm.kv_empty[s], ((jg / kStages1) - 1) & 1, a.status, ab,
+                           kSiteProducer);
+            if (!ok) break;
+          }
+          ok = load_kv_tile<kWin1, kWin1CopyStride>(sm, a, &tk, &tv, s, j, it.bh, it.h,
+                                                     128 * it.qt, jg == 0, ab);
+        }
       }
-      if (q_issued) mbar_drain(&sm.q_full[0], 0);
-      for (int j = max(0, issued - kStages1); j < issued; ++j) {
-        mbar_drain(&sm.k_full[j % kStages1], (j / kStages1) & 1);
-        mbar_drain(&sm.v_full[j % kStages1], (j / kStages1) & 1);
+      // Copies still in flight land before this CTA leaves.
+      if (q_items > 0) mbar_drain(&sm.q_full[0], (q_items - 1) & 1);
+      for (int x = max(0, jg - kStages1); x < jg; ++x) {
+        mbar_drain(&sm.k_full[x % kStages1], (x / kStages1) & 1);
+        mbar_drain(&sm.v_full[x % kStages1], (x / kStages1) & 1);
       }
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = (*ab == 0);
-      if (ok) ok = mbar_wait(&sm.q_full[0], 0, a.status, ab, kSiteMmaQ);
-      if (ok) ok = mbar_wait(&sm.k_full[0], 0, a.status, ab, kSiteMmaK);
-      if (ok) {
-        tc_fence_after();
-        issue_S(sm, tm, 0, 0, &sm.s_full[0]);
-      }
-      // Per key tile: S of the next tile once the softmax has copied this S,
-      // then PV once its probabilities are in.
-      for (int j = 0; ok && j < nKV; ++j) {
-        const int s = j % kStages1;
-        if (j + 1 < nKV) {
-          ok = mbar_wait(&sm.s_free[0], j & 1, a.status, ab, kSiteMmaSFree);
+      int jg = 0;
+      Item1 it;
+      for (int n = 0; ok && single_item(a, n, it); ++n) {
+        ok = mbar_wait(&sm.q_full[0], n & 1, a.status, ab, kSiteMmaQ);
+        if (!ok) break;
+        // The S columns are free once the softmax has copied the previous S.
+        if (jg > 0) {
+          ok = mbar_wait(&sm.s_free[0], (jg - 1) & 1, a.status, ab, kSiteMmaSFree);
           if (!ok) break;
-          ok = mbar_wait(&sm.k_full[(j + 1) % kStages1], ((j + 1) / kStages1) & 1, a.status, ab,
-                         kSiteMmaK);
+        }
+        ok = mbar_wait(&sm.k_full[jg % kStages1], (jg / kStages1) & 1, a.status, ab, kSiteMmaK);
+        if (!ok) break;
+        tc_fence_after();
+        issue_S(sm, tm, 0, jg % kStages1, &sm.s_full[0]);
+        // Q is free for the next item once the item's last S is done.
+        if (it.nKV == 1) umma_commit(&sm.q_empty);
+        // Per key tile: S of the next tile once the softmax has copied this
+        // S, then PV once its probabilities are in.
+        for (int j = 0; ok && j < it.nKV; ++j) {
+          const int g = jg + j, s = g % kStages1;
+          if (j + 1 < it.nKV) {
+            ok = mbar_wait(&sm.s_free[0], g & 1, a.status, ab, kSiteMmaSFree);
+            if (!ok) break;
+            ok = mbar_wait(&sm.k_full[(g + 1) % kStages1], ((g + 1) / kStages1) & 1, a.status,
+                           ab, kSiteMmaK);
+            if (!ok) break;
+            tc_fence_after();
+            issue_S(sm, tm, 0, (g + 1) % kStages1, &sm.s_full[0]);
+            if (j + 2 == it.nKV) umma_commit(&sm.q_empty);
+          }
+          ok = mbar_wait(&sm.v_full[s], (g / kStages1) & 1, a.status, ab, kSiteMmaV);
+          if (!ok) break;
+          ok = mbar_wait(&sm.p_full[0], g & 1, a.status, ab, kSiteMmaP);
           if (!ok) break;
           tc_fence_after();
-          issue_S(sm, tm, 0, (j + 1) % kStages1, &sm.s_full[0]);
+          issue_PV(sm, tm + 192, tm + 128, s, j == 0, &sm.pv_done[0]);
+          umma_commit(&sm.kv_empty[s]);
         }
-        ok = mbar_wait(&sm.v_full[s], (j / kStages1) & 1, a.status, ab, kSiteMmaV);
         if (!ok) break;
-        ok = mbar_wait(&sm.p_full[0], j & 1, a.status, ab, kSiteMmaP);
-        if (!ok) break;
-        tc_fence_after();
-        issue_PV(sm, tm + 192, tm + 128, s, j == 0, &sm.pv_done[0]);
-        umma_commit(&sm.kv_empty[s]);
+        jg += it.nKV;
       }
       umma_commit(&sm.mma_final);
       mbar_drain(&sm.mma_final, 0);
@@ -726,44 +772,66 @@ __global__ void __launch_bounds__(kThreads1, 2)
   } else {
     // ------------------------------------------------------------ softmax
     const int r = threadIdx.x;  // row within the tile = TMEM lane
-    const int i = i0 + r;
     const uint32_t lb = tmem_lane_base(warp);
     const uint32_t tS = tm + lb, tP = tm + lb + 128, tO = tm + lb + 192;
-    const float cr = logit_scale(a, h, i);
-    SoftRow row{-INFINITY, 0.0f, 0.0f};
-    bool ok = (*ab == 0);
-    // Column c reads window entry 128 + r - c (the first 256 entries of the
-    // 384-entry window): reversed entry kWin - 129 - r + c, one aligned
-    // 16-byte vector per four columns in copy kq.
+    // Column c reads window entry 128 + r - c: reversed entry 127 - r + c, in
+    // copy kq one aligned 16-byte vector per four columns.
     const int kq = (r + 1) & 3;
-    const int wrev = win_copy_off(kq, kWinCopyStride) + (kWin - 129 - r + kq);
-    for (int j = 0; ok && j < nKV; ++j) {
-      const int s = j % kStages1;
-      const int j0 = 128 * j;
-      const bool masked = (a.causal && (j0 + 127 > i0)) || (j0 + 128 > a.T);
-      int lim = a.T - 1 - j0;
-      if (a.causal) lim = min(lim, i - j0);
-      const TilePhases ph{static_cast<uint32_t>(j & 1), static_cast<uint32_t>((j / kStages1) & 1),
-                          j > 0, static_cast<uint32_t>((j - 1) & 1)};
-      ok = softmax_tile(sm, row, 0, s, ph, sm.win[s] + wrev, cr, masked, lim, j > 0, tS, tP, tO,
-                        a.status, ab, lane);
-    }
-    if (ok) ok = warp_wait(&sm.pv_done[0], (nKV - 1) & 1, a.status, ab, kSiteSoftEnd);
-    if (ok) {
-      // Every S and PV product is done: the K stages are free for the O
-      // staging tile.
-      tc_fence_after();
-      uint8_t* ost = sm.k[0];
-      const float inv_l = 1.0f / row.l;
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        uint32_t ov[32];
-        tmem_ld_32x32b_x32(tO + 32 * hb, ov);
-        tmem_ld_wait();
-        reg_fence32(ov);
-        stage_half(a, ost, ov, hb, inv_l, r);
+    const int wrev = win_copy_off(kq, kWin1CopyStride) + (kWin1 - 129 - r + kq);
+    bool ok = (*ab == 0);
+    int jg = 0, boxes = 0;
+    Item1 it;
+    for (int n = 0; ok && single_item(a, n, it); ++n) {
+      const int i0 = 128 * it.qt, i = i0 + r;
+      const float cr = logit_scale(a, it.h, i);
+      SoftRow row{-INFINITY, 0.0f, 0.0f};
+      for (int j = 0; ok && j < it.nKV; ++j) {
+        const int g = jg + j, s = g % kStages1;
+        const int j0 = 128 * j;
+        const bool masked = (a.causal && (j0 + 127 > i0)) || (j0 + 128 > a.T);
+        int lim = a.T - 1 - j0;
+        if (a.causal) lim = min(lim, i - j0);
+        const TilePhases ph{static_cast<uint32_t>(g & 1),
+                            static_cast<uint32_t>((g / kStages1) & 1), j > 0,
+                            static_cast<uint32_t>((g - 1) & 1)};
+        ok = softmax_tile(sm, row, 0, s, ph, sm.win[s] + wrev, cr, masked, lim, j > 0, tS, tP, tO,
+                          a.status, ab, lane);
       }
-      finish_store(a, &to, ost, &sm.o_full[0], 0, row, i, i0, bh, warp, lane, ab);
+      jg += it.nKV;
+      if (ok) ok = warp_wait(&sm.pv_done[0], (jg - 1) & 1, a.status, ab, kSiteSoftEnd);
+      if (!ok) break;
+      // O leaves box by box through the staging tile: fp32 as two boxes of
+      // 32 columns, bf16 as one of 64.
+      tc_fence_after();
+      const float inv_l = 1.0f / row.l;
+      const int nbox = a.o_fp32 ? 2 : 1;
+      for (int bx = 0; ok && bx < nbox; ++bx, ++boxes) {
+        if (boxes > 0) {
+          ok = warp_wait(&sm.ost_free, (boxes - 1) & 1, a.status, ab, kSiteSoftStore);
+          if (!ok) break;
+        }
+        for (int hb = (a.o_fp32 ? bx : 0); hb < (a.o_fp32 ? bx + 1 : 2); ++hb) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(tO + 32 * hb, ov);
+          tmem_ld_wait();
+          reg_fence32(ov);
+          stage_half(a, sm.ost, ov, hb, inv_l, r, 0);
+        }
+        if (bx == 0 && i < a.T && a.lse)
+          a.lse[static_cast<int64_t>(it.bh) * a.T + i] = (row.m + __log2f(row.le)) * kLn2f;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.o_full[0]);
+        if (warp == 0 && lane == 0) {
+          if (mbar_wait(&sm.o_full[0], boxes & 1, a.status, ab, kSiteSoftStore) &&
+              store_row_ok(i0, a.T, a.status, ab, kSiteOutRow)) {
+            tma_store_3d(&to, sm.ost, a.o_fp32 ? 32 * bx : 0, i0, it.bh);
+            bulk_commit();
+            bulk_wait_read_all();  // the staging box may be written again
+          }
+          mbar_arrive(&sm.ost_free);
+        }
+      }
     }
   }
 
@@ -793,13 +861,14 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     attr_set = true;
   }
   // Paired CTAs (256 rows, one per SM) when they fill at least two waves of
-  // the SMs; otherwise single-tile CTAs, two per SM.
+  // the SMs; otherwise the persistent single-tile grid, two CTAs per SM.
   const long bh = static_cast<long>(a.B) * a.H;
   const long paired = static_cast<long>((a.T + 255) / 256) * bh;
   int sms = sm_count();
   if (sms <= 0) sms = 148;
   if (paired < 2L * sms) {
-    const unsigned grid = static_cast<unsigned>(((a.T + 127) / 128) * bh);
+    const long items = static_cast<long>((a.T + 127) / 128) * bh;
+    const unsigned grid = static_cast<unsigned>(items < 2L * sms ? items : 2L * sms);
     return launch_k(bam_fwd_single_kernel, dim3(grid), dim3(kThreads1), smem1, st, true, tq, tk,
                     tv, to, a);
   }
