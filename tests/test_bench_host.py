@@ -58,11 +58,17 @@ def test_flop_count():
     assert bench.pairs_causal(8, 12, 512) == 8 * 12 * 512 * 513 // 2
 
 
-def test_kernel_hashes_are_per_kernel():
+def test_kernel_hashes_are_per_source_set():
+    # Kernels built from the same files (the two forward kernels share fwd.cu)
+    # share a hash; different source sets, and the whole tree, differ.
     hs = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_SOURCES}
-    hs["all"] = bench.kernel_source_hash()
-    assert len(set(hs.values())) == len(hs)
-    for h in hs.values():
+    by_sources = {}
+    for k, h in hs.items():
+        by_sources.setdefault(bench.KERNEL_SOURCES[k], set()).add(h)
+    assert all(len(v) == 1 for v in by_sources.values())
+    distinct = {next(iter(v)) for v in by_sources.values()} | {bench.kernel_source_hash()}
+    assert len(distinct) == len(by_sources) + 1
+    for h in distinct:
         assert len(h) == 16 and int(h, 16) >= 0
 
 

@@ -68,10 +68,17 @@ def sharded_attention_backward(q, k, v, o, lse, dO, alpha, beta, mu, s=None, *, 
 
 
 def allreduce_head_grads(grads, dist, group=None):
-    """Sum the per-head scalar gradients over ranks, in place (one collective)."""
+    """Sum the per-head scalar gradients over ranks, in place (one collective
+    of 4 H floats).  With the gloo backend, device tensors are reduced
+    through one host copy (gloo reduces host memory)."""
     import torch
     flat = torch.cat([g.reshape(-1) for g in grads])
-    dist.all_reduce(flat, op=dist.ReduceOp.SUM, group=group)
+    if flat.is_cuda and dist.get_backend(group) == "gloo":
+        host = flat.cpu()
+        dist.all_reduce(host, op=dist.ReduceOp.SUM, group=group)
+        flat.copy_(host)
+    else:
+        dist.all_reduce(flat, op=dist.ReduceOp.SUM, group=group)
     off = 0
     for g in grads:
         n = g.numel()
