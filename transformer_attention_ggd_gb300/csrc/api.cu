@@ -66,17 +66,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// [BH, T, 64] bf16 viewed as a 3-D tensor (64, T, BH); 128 x 64 boxes with
-// the 128-byte swizzle that the tcgen05 K-major / MN-major operands expect.
-// Rows past T inside a head read as zeros.
-bool encode_rows(CUtensorMap* m, const void* base, int BH, int T) {
+// [BH, T, 64] bf16 viewed as a 3-D tensor (64, T, BH); boxes of `rows` x 64
+// (128 by default) with the 128-byte swizzle that the tcgen05 K-major /
+// MN-major operands expect.  Rows past T inside a head read as zeros.
+bool encode_rows(CUtensorMap* m, const void* base, int BH, int T, unsigned rows = 128) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(T),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
                            static_cast<cuuint64_t>(T) * kHeadDim * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -84,16 +84,17 @@ bool encode_rows(CUtensorMap* m, const void* base, int BH, int T) {
   return r == CUDA_SUCCESS;
 }
 
-// fp32 [BH, T, 64] accumulator as a 3-D tensor (64, T, BH) in 32 x 128
-// boxes (128-byte rows, 128-byte swizzle) for TMA reductions.
-bool encode_acc_rows(CUtensorMap* m, void* base, int BH, int T) {
+// fp32 [BH, T, 64] accumulator as a 3-D tensor (64, T, BH) in boxes of 32
+// columns x `rows` (128 by default; 128-byte rows, 128-byte swizzle) for TMA
+// reductions and stores.
+bool encode_acc_rows(CUtensorMap* m, void* base, int BH, int T, unsigned rows = 128) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(T),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 4,
                            static_cast<cuuint64_t>(T) * kHeadDim * 4};
-  cuuint32_t box[3] = {32, 128, 1};
+  cuuint32_t box[3] = {32, rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -367,11 +368,15 @@ bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, in
   fa.o_fp32 = o_fp32 ? 1 : 0;
   fa.tab_len = g.len;
   fa.tab_off = g.off;
-  // O by TMA stores: fp32 in 32-column boxes, bf16 in 64-column boxes.
-  CUtensorMap to;
-  if (!(o_fp32 ? encode_acc_rows(&to, o, BH, T) : encode_rows(&to, o, BH, T))) return BAM_ERR_CUDA;
+  // O by TMA stores: fp32 in 32-column boxes, bf16 in 64-column boxes; 128
+  // rows a box for the paired kernel, 32 (one warp's rows) for the
+  // single-tile kernel.
+  CUtensorMap to, to32;
+  if (!(o_fp32 ? encode_acc_rows(&to, o, BH, T) : encode_rows(&to, o, BH, T)) ||
+      !(o_fp32 ? encode_acc_rows(&to32, o, BH, T, 32) : encode_rows(&to32, o, BH, T, 32)))
+    return BAM_ERR_CUDA;
   e = launch_kernel(BAM_KERNEL_FWD, stream,
-                    [&] { return launch_fwd(tq, tk, tv, to, fa, stream); });
+                    [&] { return launch_fwd(tq, tk, tv, to, to32, fa, stream); });
   return cuda_status(e);
 }
 

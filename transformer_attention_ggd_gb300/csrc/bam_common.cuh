@@ -179,8 +179,11 @@ inline int sm_count() {
 
 // Internal launchers (one per kernel).  Each returns the launch error.
 cudaError_t launch_table(const TableArgs& a, cudaStream_t st);
+// `to`: O in 128-row boxes (paired kernel); `to32`: O in 32-row boxes, one
+// warp's rows (single-tile kernel).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
+                       const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a,
+                       cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st);

@@ -605,7 +605,7 @@ struct __align__(1024) Fwd1Smem {
   uint8_t q[1][kTileBytes];
   uint8_t k[kStages1][kTileBytes];
   uint8_t v[kStages1][kTileBytes];
-  uint8_t ost[kTileBytes];  // one 128-byte-swizzled box of O rows for a TMA store
+  uint8_t ost[kTileBytes];  // per softmax warp, one 32-row 128-byte-swizzled box of O
   float win[kStages1][kWin1Stage];
   uint64_t q_full[1];
   uint64_t q_empty;   // the item's S products are done with its Q
@@ -616,8 +616,6 @@ struct __align__(1024) Fwd1Smem {
   uint64_t s_free[1];
   uint64_t p_full[1];
   uint64_t pv_done[1];
-  uint64_t o_full[1];  // the four softmax warps have staged a box
-  uint64_t ost_free;   // the staged box has been read by its TMA store
   uint64_t mma_final;
   uint32_t tmem_base;
   int abort_flag;
@@ -667,8 +665,6 @@ __global__ void __launch_bounds__(kThreads1, 2)
     mbar_init(&sm.s_free[0], 4);
     mbar_init(&sm.p_full[0], 4);
     mbar_init(&sm.pv_done[0], 1);
-    mbar_init(&sm.o_full[0], 4);
-    mbar_init(&sm.ost_free, 1);
     mbar_init(&sm.mma_final, 1);
     fence_barrier_init();
   }
@@ -800,39 +796,39 @@ __global__ void __launch_bounds__(kThreads1, 2)
       jg += it.nKV;
       if (ok) ok = warp_wait(&sm.pv_done[0], (jg - 1) & 1, a.status, ab, kSiteSoftEnd);
       if (!ok) break;
-      // O leaves box by box through the staging tile: fp32 as two boxes of
-      // 32 columns, bf16 as one of 64.
+      // O leaves through this warp's quarter of the staging tile, one
+      // 32-row box per TMA store issued by the warp itself (no hand-off
+      // between warps): fp32 as two boxes of 32 columns, bf16 as one of 64.
+      // A box is staged once the warp's previous store has read the quarter.
       tc_fence_after();
       const float inv_l = 1.0f / row.l;
       const int nbox = a.o_fp32 ? 2 : 1;
-      for (int bx = 0; ok && bx < nbox; ++bx, ++boxes) {
+      const int rw = i0 + 32 * warp;  // first row of this warp's box
+      uint8_t* quarter = sm.ost + warp * (kTileBytes / 4);
+      for (int bx = 0; bx < nbox; ++bx, ++boxes) {
         if (boxes > 0) {
-          ok = warp_wait(&sm.ost_free, (boxes - 1) & 1, a.status, ab, kSiteSoftStore);
-          if (!ok) break;
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
         }
         for (int hb = (a.o_fp32 ? bx : 0); hb < (a.o_fp32 ? bx + 1 : 2); ++hb) {
           uint32_t ov[32];
           tmem_ld_32x32b_x32(tO + 32 * hb, ov);
           tmem_ld_wait();
           reg_fence32(ov);
-          stage_half(a, sm.ost, ov, hb, inv_l, r, 0);
+          stage_half(a, quarter, ov, hb, inv_l, r & 31, 0);
         }
         if (bx == 0 && i < a.T && a.lse)
           a.lse[static_cast<int64_t>(it.bh) * a.T + i] = (row.m + __log2f(row.le)) * kLn2f;
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.o_full[0]);
-        if (warp == 0 && lane == 0) {
-          if (mbar_wait(&sm.o_full[0], boxes & 1, a.status, ab, kSiteSoftStore) &&
-              store_row_ok(i0, a.T, a.status, ab, kSiteOutRow)) {
-            tma_store_3d(&to, sm.ost, a.o_fp32 ? 32 * bx : 0, i0, it.bh);
-            bulk_commit();
-            bulk_wait_read_all();  // the staging box may be written again
-          }
-          mbar_arrive(&sm.ost_free);
+        if (lane == 0 && rw < a.T && store_row_ok(rw, a.T, a.status, ab, kSiteOutRow)) {
+          tma_store_3d(&to, quarter, a.o_fp32 ? 32 * bx : 0, rw, it.bh);
+          bulk_commit();
         }
       }
     }
+    // The staging quarter stays valid until this warp's last store has read it.
+    if (lane == 0) bulk_wait_read_all();
   }
 
   tc_fence_before();
@@ -846,7 +842,8 @@ __global__ void __launch_bounds__(kThreads1, 2)
 }  // namespace
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
+                       const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a,
+                       cudaStream_t st) {
   const size_t smem = sizeof(FwdSmem) + 1024, smem1 = sizeof(Fwd1Smem) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -870,7 +867,7 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     const long items = static_cast<long>((a.T + 127) / 128) * bh;
     const unsigned grid = static_cast<unsigned>(items < 2L * sms ? items : 2L * sms);
     return launch_k(bam_fwd_single_kernel, dim3(grid), dim3(kThreads1), smem1, st, true, tq, tk,
-                    tv, to, a);
+                    tv, to32, a);
   }
   return launch_k(bam_fwd_kernel, dim3(static_cast<unsigned>(paired)), dim3(kThreads), smem, st,
                   true, tq, tk, tv, to, a);
