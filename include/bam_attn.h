@@ -239,6 +239,18 @@ bam_status bam_attn_decode_noalloc_check_status(cudaStream_t stream);
  * (debug build only; BAM_ERR_UNSUPPORTED otherwise). */
 bam_status bam_attn_debug_arm_giveup_noalloc(int n);
 
+/* Work schedule of the causal backward's persistent grid (host only:
+ * launches nothing, needs no GPU; for tests and tools).  With `grid` CTAs
+ * (the backward uses min(grid, B*H*ceil(T/128)) of them, grid = the SM
+ * count), CTA c runs items item[start[c]] .. item[start[c+1]-1] in that
+ * order; item w is key tile w / (B*H) of (b, h) = w % (B*H).  `start` holds
+ * at least min(grid, items) + 1 ints, `item` at least max_items.  Returns the
+ * number of scheduled items; 0 when the kernel deals the items out
+ * round-robin itself (non-causal, too many items, or no better makespan);
+ * -1 on a bad argument or when max_items is too small. */
+int bam_attn_bwd_schedule(int B, int H, int T, int causal, int grid, int* start, int* item,
+                          int max_items);
+
 /* Kernels that bam_attn_profile_events can bracket. */
 enum {
   BAM_KERNEL_TABLE = 0,      /* distance-table kernel (fwd, decode)        */

@@ -68,6 +68,7 @@ EXPORTED = (
     "bam_attn_debug_build",
     "bam_attn_debug_arm_giveup",
     "bam_attn_debug_arm_giveup_noalloc",
+    "bam_attn_bwd_schedule",
 )
 
 # Size of the fixed device scratch of bam_attn_decode_noalloc.
@@ -144,6 +145,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.bam_attn_debug_arm_giveup.argtypes = [vp, i]
         lib.bam_attn_debug_arm_giveup_noalloc.restype = i
         lib.bam_attn_debug_arm_giveup_noalloc.argtypes = [i]
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.bam_attn_bwd_schedule.restype = i
+        lib.bam_attn_bwd_schedule.argtypes = [i, i, i, i, i, ip, ip, i]
         _lib = lib
         return lib
 
@@ -461,6 +465,25 @@ def bam_attn_profile_events(which: int, before=None, after=None) -> None:
 
 def bam_attn_launch_count() -> int:
     return int(load_library().bam_attn_launch_count())
+
+
+def bam_attn_bwd_schedule(B: int, H: int, T: int, causal: bool, grid: int):
+    """The causal backward's per-CTA item lists for `grid` CTAs (host only):
+    a list of item-index lists, CTA by CTA, or None when the kernel deals
+    items out round-robin itself.  Item w is key tile w // (B*H) of
+    (b, h) = w % (B*H)."""
+    nkb = (T + 127) // 128
+    total = nkb * B * H
+    g = min(grid, total)
+    start = (ctypes.c_int * (g + 1))()
+    item = (ctypes.c_int * max(total, 1))()
+    n = int(load_library().bam_attn_bwd_schedule(int(B), int(H), int(T), int(bool(causal)),
+                                                 int(grid), start, item, total))
+    if n < 0:
+        raise BamError(BAM_ERR_INVALID_ARG, "bam_attn_bwd_schedule")
+    if n == 0:
+        return None
+    return [list(item[start[c]:start[c + 1]]) for c in range(g)]
 
 
 # ---------------------------------------------------------------- allocating helpers

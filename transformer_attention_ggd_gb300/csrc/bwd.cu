@@ -45,7 +45,11 @@
 //              warps on its scheduler.
 // TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
 //               dK [384,448) dV [448,512).
+#include <algorithm>
+#include <climits>
+#include <mutex>
 #include <type_traits>
+#include <vector>
 
 #include "table_eval.cuh"
 
@@ -151,18 +155,38 @@ __device__ __forceinline__ uint32_t mn_chunk_offset(int m8, int k) {
   return (m8 >> 3) * kTile + (k >> 3) * 1024 + (k & 7) * 128 + (((m8 & 7) ^ (k & 7)) << 4);
 }
 
-// Work item w of a persistent CTA: key tile kb of head bh.  Items are in
-// longest-first order (causal: kb = 0 sees every query tile) and dealt out in
+// Work item w of a persistent CTA: key tile kb of head bh (item index
+// kb * B * H + bh; causal: kb = 0 sees every query tile).  With a schedule
+// (BwdSched::n > 0) CTA c takes items item[start[c]] .. item[start[c+1]-1]
+// in that order; otherwise items are taken longest first and dealt out in
 // rounds, alternating direction ("snake") so that long and short items mix.
 struct BwdItem {
   int kb, bh, h, j0, q_first, nq;
 };
 
-__device__ __forceinline__ bool bwd_item(const BwdArgs& a, int round, BwdItem& it) {
+// Per-CTA item lists, passed by value as a kernel parameter (2.4 KB; larger
+// problems keep the round-robin deal).
+constexpr int kSchedMaxCtas = 160;
+constexpr int kSchedMaxItems = 1024;
+struct BwdSched {
+  int n;  // scheduled items; 0: the kernel deals them out itself
+  uint16_t start[kSchedMaxCtas + 1];
+  uint16_t item[kSchedMaxItems];
+};
+
+__device__ __forceinline__ bool bwd_item(const BwdArgs& a, const BwdSched& sc, int round,
+                                         BwdItem& it) {
   const int BH = a.B * a.H;
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  const int idx = round * G + ((round & 1) ? (G - 1 - c) : c);
-  if (idx >= a.nkb * BH) return false;
+  int idx;
+  if (sc.n > 0) {
+    const int p = sc.start[c] + round;
+    if (p >= sc.start[c + 1]) return false;
+    idx = sc.item[p];
+  } else {
+    idx = round * G + ((round & 1) ? (G - 1 - c) : c);
+    if (idx >= a.nkb * BH) return false;
+  }
   it.kb = idx / BH;
   it.bh = idx % BH;
   it.h = it.bh % a.H;
@@ -176,7 +200,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
     bam_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
-                   const __grid_constant__ CUtensorMap tdv, const BwdArgs a) {
+                   const __grid_constant__ CUtensorMap tdv, const BwdArgs a,
+                   const __grid_constant__ BwdSched sc) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // Aligned by an offset from the shared array itself (not through an
   // integer cast), so that accesses stay in the shared address space.
@@ -237,7 +262,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       prefetch_tmap(&tv);
       prefetch_tmap(&tdo);
       BwdItem it;
-      for (int round = 0; ok && bwd_item(a, round, it); ++round) {
+      for (int round = 0; ok && bwd_item(a, sc, round, it); ++round) {
         for (int t = 0; ok && t < it.nq; ++t, ++g) {
           const int s = g % kBStages;
           const int i0 = (it.q_first + t) * 128;
@@ -330,14 +355,14 @@ __global__ void __launch_bounds__(kBThreads, 1)
       };
       int g = 0, n = 0;
       BwdItem it, nxt;
-      bool have = bwd_item(a, 0, it);
+      bool have = bwd_item(a, sc, 0, it);
       if (ok && have) {
         ok = mbar_wait(&sm.kv_full, 0, a.status, ab, kSiteBMmaKV);
         if (ok) ok = issue_s_dp(0);
         if (ok && it.nq == 1) umma_commit(&sm.v_empty);  // that was the item's last dP
       }
       for (int round = 0; ok && have; ++round) {
-        const bool have_next = bwd_item(a, round + 1, nxt);
+        const bool have_next = bwd_item(a, sc, round + 1, nxt);
         for (int t = 0; ok && t < it.nq; ++t, ++g) {
           const int s = g % kBStages;
           // S and dP of the item's next tile once this tile's S/dP columns
@@ -392,7 +417,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       bool ok = (*ab == 0);
       int g = 0;
       BwdItem it;
-      for (int round = 0; ok && bwd_item(a, round, it); ++round) {
+      for (int round = 0; ok && bwd_item(a, sc, round, it); ++round) {
         for (int t = 0; ok && t < it.nq; ++t, ++g) {
           ok = mbar_wait(&sm.dqs_full, g & 1, a.status, ab, kSiteBDq);
           if (!ok) break;
@@ -472,7 +497,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       if (h_ >= 0) s_nx = a.ssmax ? __ldg(a.s + h_) : 1.0f;
     };
     BwdItem it;
-    bool have = bwd_item(a, 0, it);
+    bool have = bwd_item(a, sc, 0, it);
     if (have) prefetch_row(it.bh, it.q_first * 128 + r, it.h);
     for (int round = 0; ok && have; ++round) {
       const int bh = it.bh, j0 = it.j0, q_first = it.q_first, nq = it.nq;
@@ -492,7 +517,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
           prefetch_row(bh, i + 128, -1);
         } else {
           BwdItem nxt;
-          if (bwd_item(a, round + 1, nxt)) prefetch_row(nxt.bh, nxt.q_first * 128 + r, nxt.h);
+          if (bwd_item(a, sc, round + 1, nxt)) prefetch_row(nxt.bh, nxt.q_first * 128 + r, nxt.h);
         }
         // Per-row constants.
         const float n = a.causal ? static_cast<float>(i + 1) : static_cast<float>(a.T);
@@ -714,7 +739,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
           if (lane == 0) mbar_arrive(&sm.epi_full);
         }
       }
-      have = bwd_item(a, round + 1, it);
+      have = bwd_item(a, sc, round + 1, it);
     }
     // A warp that gave up inside a tile may still have TMEM stores in
     // flight; they complete before the columns are freed.
@@ -875,6 +900,206 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
   }
 }
 
+// Host: per-CTA item lists for the causal backward.  Item costs in units of
+// ~0.3 us: 11 per query tile, 8 per item boundary (~3.3 and ~2.4 us measured
+// on the B=8 H=12 T=512 training workload).  First-fit decreasing packs the
+// items, longest first, each into the first CTA where it fits under a
+// makespan bound, and bisection finds the smallest bound that packs.  A local
+// search then empties the makespan level CTA by CTA (moving one item, or
+// swapping one item for one or two, between a CTA at the makespan and one
+// below it, neither ending at or above it), which spreads the long CTAs: on
+// the training workload first-fit leaves 96 CTAs with 4+3 query tiles and the
+// search halves that (48 x 4+3, 48 x 4+1+1, 24 x 3+3, 32 x 2+2+2), which ran
+// 1.5 us faster.  The lists are used when their makespan beats that of the
+// round-robin snake (n = 0 otherwise).
+constexpr long kTileCost = 11, kBoundaryCost = 8;
+
+long list_cost(long tiles, size_t items) {
+  return tiles * kTileCost + (items > 0 ? static_cast<long>(items - 1) * kBoundaryCost : 0);
+}
+
+long snake_makespan(int BH, int nkb, int G) {
+  std::vector<long> tiles(G, 0);
+  std::vector<size_t> items(G, 0);
+  const int total = BH * nkb;
+  for (int r = 0; r * G < total; ++r)
+    for (int c = 0; c < G; ++c) {
+      const int idx = r * G + ((r & 1) ? (G - 1 - c) : c);
+      if (idx >= total) continue;
+      tiles[c] += nkb - idx / BH;
+      ++items[c];
+    }
+  long m = 0;
+  for (int c = 0; c < G; ++c) m = std::max(m, list_cost(tiles[c], items[c]));
+  return m;
+}
+
+// First-fit decreasing under makespan bound M: the sizes (query tiles) of the
+// items each CTA runs.
+bool pack_sizes(int BH, int nkb, int G, long M, std::vector<std::vector<int>>& per) {
+  per.assign(G, {});
+  std::vector<long> load(G, 0);
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int size = nkb - kb;
+    for (int bh = 0; bh < BH; ++bh) {
+      int c = 0;
+      for (; c < G; ++c) {
+        const long add = size * kTileCost + (per[c].empty() ? 0 : kBoundaryCost);
+        if (load[c] + add <= M) {
+          load[c] += add;
+          per[c].push_back(size);
+          break;
+        }
+      }
+      if (c == G) return false;
+    }
+  }
+  return true;
+}
+
+// The local search described above, with at most `budget` candidate
+// evaluations.  Each accepted change lowers the number of CTAs at the
+// makespan, so the search ends.
+void spread_makespan(std::vector<std::vector<int>>& per, long budget) {
+  const int G = static_cast<int>(per.size());
+  std::vector<long> tiles(G, 0);
+  for (int c = 0; c < G; ++c)
+    for (int x : per[c]) tiles[c] += x;
+  while (budget > 0) {
+    long m = 0;
+    for (int c = 0; c < G; ++c) m = std::max(m, list_cost(tiles[c], per[c].size()));
+    bool changed = false;
+    for (int a = 0; a < G && !changed && budget > 0; ++a) {
+      const size_t na = per[a].size();
+      if (list_cost(tiles[a], na) != m) continue;
+      long best = LONG_MAX;
+      int kind = -1, bb = -1;
+      size_t bi = 0, bj = 0, bk = 0;
+      for (int b = 0; b < G; ++b) {
+        if (b == a) continue;
+        const size_t nb = per[b].size();
+        const long lb = list_cost(tiles[b], nb);
+        if (lb >= m) continue;
+        const long base = m * m + lb * lb;
+        auto consider = [&](long ca, long cb, int k, size_t i, size_t j, size_t l) {
+          if (ca >= m || cb >= m) return;
+          const long d = ca * ca + cb * cb - base;
+          if (d < best) {
+            best = d;
+            kind = k;
+            bb = b;
+            bi = i;
+            bj = j;
+            bk = l;
+          }
+        };
+        for (size_t i = 0; i < na; ++i) {
+          const int si = per[a][i];
+          consider(list_cost(tiles[a] - si, na - 1), list_cost(tiles[b] + si, nb + 1), 0, i, 0, 0);
+          for (size_t j = 0; j < nb; ++j) {
+            const int sj = per[b][j];
+            if (sj != si)
+              consider(list_cost(tiles[a] - si + sj, na), list_cost(tiles[b] - sj + si, nb), 1, i,
+                       j, 0);
+            if (nb > 12) continue;
+            for (size_t l = j + 1; l < nb; ++l) {
+              const int sl = per[b][l];
+              consider(list_cost(tiles[a] - si + sj + sl, na + 1),
+                       list_cost(tiles[b] - sj - sl + si, nb - 1), 2, i, j, l);
+            }
+          }
+          budget -= static_cast<long>(nb * nb / 2 + nb + 1);
+        }
+      }
+      if (kind < 0) continue;
+      std::vector<int>& A = per[a];
+      std::vector<int>& Bv = per[bb];
+      const int si = A[bi];
+      if (kind == 0) {
+        A.erase(A.begin() + bi);
+        Bv.push_back(si);
+        tiles[a] -= si;
+        tiles[bb] += si;
+      } else if (kind == 1) {
+        const int sj = Bv[bj];
+        A[bi] = sj;
+        Bv[bj] = si;
+        tiles[a] += sj - si;
+        tiles[bb] += si - sj;
+      } else {
+        const int sj = Bv[bj], sl = Bv[bk];
+        A[bi] = sj;
+        A.push_back(sl);
+        Bv.erase(Bv.begin() + bk);  // bk > bj: erase the later one first
+        Bv.erase(Bv.begin() + bj);
+        Bv.push_back(si);
+        tiles[a] += sj + sl - si;
+        tiles[bb] += si - sj - sl;
+      }
+      changed = true;
+    }
+    if (!changed) return;
+  }
+}
+
+bool build_schedule(int BH, int nkb, int G, BwdSched& sc) {
+  const int total = BH * nkb;
+  sc.n = 0;
+  if (total > kSchedMaxItems || G > kSchedMaxCtas || G < 1 || total < G) return false;
+  long sum = 0;
+  for (int kb = 0; kb < nkb; ++kb) sum += static_cast<long>(nkb - kb) * BH * kTileCost;
+  sum += static_cast<long>(total - G) * kBoundaryCost;
+  long lo = std::max((sum + G - 1) / G, static_cast<long>(nkb) * kTileCost);
+  long hi = snake_makespan(BH, nkb, G) - 1;  // only a strictly better bound is of use
+  std::vector<std::vector<int>> per, best;
+  while (lo <= hi) {
+    const long mid = lo + (hi - lo) / 2;
+    if (pack_sizes(BH, nkb, G, mid, per)) {
+      best = per;
+      hi = mid - 1;
+    } else {
+      lo = mid + 1;
+    }
+  }
+  if (best.empty()) return false;
+  spread_makespan(best, 50000000L);
+  // Concrete items: within a size class, heads in CTA order; each CTA's items
+  // longest first.
+  std::vector<int> next_bh(nkb + 1, 0);
+  int n = 0;
+  for (int c = 0; c < G; ++c) {
+    std::sort(best[c].begin(), best[c].end(), [](int x, int y) { return x > y; });
+    sc.start[c] = static_cast<uint16_t>(n);
+    for (int size : best[c]) sc.item[n++] = static_cast<uint16_t>((nkb - size) * BH + next_bh[size]++);
+  }
+  sc.start[G] = static_cast<uint16_t>(n);
+  sc.n = n;
+  return n == total;
+}
+
+// The schedule for this shape into `out` (n = 0: none).  Schedules of recent
+// shapes are kept, so the host cost is paid once per shape.
+void schedule_for(int BH, int nkb, int causal, int G, BwdSched& out) {
+  struct Entry {
+    int BH, nkb, G;
+    BwdSched sc;
+  };
+  out.n = 0;
+  if (!causal) return;
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : cache)
+    if (e.BH == BH && e.nkb == nkb && e.G == G) {
+      out = e.sc;
+      return;
+    }
+  if (cache.size() >= 8) cache.erase(cache.begin());
+  cache.push_back(Entry{BH, nkb, G, {}});
+  build_schedule(BH, nkb, G, cache.back().sc);
+  out = cache.back().sc;
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t st) {
@@ -912,8 +1137,10 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   }
   const long items = static_cast<long>(a.nkb) * a.B * a.H;
   const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
+  BwdSched sc;
+  schedule_for(a.B * a.H, a.nkb, a.causal, static_cast<int>(grid), sc);
   return launch_k(bam_bwd_kernel, dim3(grid), dim3(kBThreads), smem, st, true, tq, tk, tv, tdo,
-                  tdq, tdk, tdv, a);
+                  tdq, tdk, tdv, a, sc);
 }
 
 cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
@@ -929,3 +1156,19 @@ cudaError_t launch_bwd_final(const BwdArgs& a, cudaStream_t st) {
 }
 
 }  // namespace bam
+
+extern "C" int bam_attn_bwd_schedule(int B, int H, int T, int causal, int grid, int* start,
+                                     int* item, int max_items) {
+  if (B < 1 || H < 1 || T < 1 || grid < 1 || !start || !item || max_items < 0) return -1;
+  const int nkb = (T + 127) / 128;
+  const long items = static_cast<long>(nkb) * B * H;
+  if (items > 0x7fffffffL / 2) return -1;
+  const int G = static_cast<int>(items < grid ? items : grid);
+  bam::BwdSched sc;
+  bam::schedule_for(B * H, nkb, causal, G, sc);
+  if (sc.n == 0) return 0;
+  if (sc.n > max_items) return -1;
+  for (int c = 0; c <= G; ++c) start[c] = sc.start[c];
+  for (int w = 0; w < sc.n; ++w) item[w] = sc.item[w];
+  return sc.n;
+}
