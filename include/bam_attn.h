@@ -43,11 +43,9 @@
  *    bam_attn_check_status().  A recorded error stays until it is read: a
  *    later call on the same workspace runs normally but neither erases nor
  *    overwrites it (the first error since the last check is reported).
- *  - One device per process (one process per GPU, as torch.distributed
- *    launches ranks): the kernels' shared-memory limits are raised once, on
- *    the device current at the first call.  On another device of the same
- *    process the launch of the first kernel that needs the raised limit is
- *    refused and the call returns BAM_ERR_CUDA.
+ *  - A call runs on the device current at the call.  The kernels'
+ *    shared-memory limits are raised once per device and the SM count is
+ *    read once per device, so one process may drive several GPUs.
  */
 #ifndef BAM_ATTN_H_
 #define BAM_ATTN_H_

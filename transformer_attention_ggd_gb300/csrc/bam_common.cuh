@@ -177,6 +177,22 @@ inline int sm_count() {
   return cached[dev];
 }
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (the attribute belongs to the device's context).
+// `done` is the caller's per-kernel flag array.
+template <typename F>
+cudaError_t smem_limit_once(F* kernel, size_t bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes));
+  if (e == cudaSuccess && cached) done[dev] = true;
+  return e;
+}
+
 // Internal launchers (one per kernel).  Each returns the launch error.
 cudaError_t launch_table(const TableArgs& a, cudaStream_t st);
 // `to`: O in 128-row boxes (paired kernel); `to32`: O in 32-row boxes, one

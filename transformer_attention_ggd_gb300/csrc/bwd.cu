@@ -1119,22 +1119,12 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(BwdSmem) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bam_bwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool limit_set[64] = {};
+  cudaError_t e = smem_limit_once(bam_bwd_kernel, smem, limit_set);
+  if (e != cudaSuccess) return e;
   // Persistent: one CTA per SM (at most one per work item).
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-  }
+  const int num_sms = sm_count();
+  if (num_sms <= 0) return cudaErrorInvalidDevice;
   const long items = static_cast<long>(a.nkb) * a.B * a.H;
   const unsigned grid = static_cast<unsigned>(items < num_sms ? items : num_sms);
   BwdSched sc;

@@ -331,14 +331,9 @@ void decode_split(int BH, int Tkv, int* nsplit, int* chunk) {
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(DecSmem) + 128;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bam_decode_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool limit_set[64] = {};
+  const cudaError_t e = smem_limit_once(bam_decode_kernel, smem, limit_set);
+  if (e != cudaSuccess) return e;
   dim3 grid(a.nsplit, a.B * a.H);
   return launch_k(bam_decode_kernel, grid, dim3(kDecThreads), smem, st, true, a);
 }

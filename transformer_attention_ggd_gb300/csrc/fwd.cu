@@ -845,18 +845,10 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& to, const CUtensorMap& to32, const FwdArgs& a,
                        cudaStream_t st) {
   const size_t smem = sizeof(FwdSmem) + 1024, smem1 = sizeof(Fwd1Smem) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bam_fwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(bam_fwd_single_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem1));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool paired_set[64] = {}, single_set[64] = {};
+  cudaError_t e = smem_limit_once(bam_fwd_kernel, smem, paired_set);
+  if (e == cudaSuccess) e = smem_limit_once(bam_fwd_single_kernel, smem1, single_set);
+  if (e != cudaSuccess) return e;
   // Paired CTAs (256 rows, one per SM) when they fill at least two waves of
   // the SMs; otherwise the persistent single-tile grid, two CTAs per SM.
   const long bh = static_cast<long>(a.B) * a.H;
