@@ -84,6 +84,20 @@ def test_config2_training_step_full():
     _compare(got, ref, True)
 
 
+@pytest.mark.parametrize("B,H,T", [(16, 16, 512), (7, 11, 520)])
+def test_packed_schedules_full(B, H, T):
+    """Shapes whose work items run in host-packed per-CTA lists (1024 items,
+    the largest the kernel parameter holds, and a ragged T with few heads):
+    every output against the oracle."""
+    assert ba.bam_attn_bwd_schedule(B, H, T, True, 152) is not None
+    rng = np.random.default_rng(B * 1000 + T)
+    bits = {n: normal_bits(rng, (B, H, T, 64)) for n in ("q", "k", "v", "do")}
+    prm = random_params(H, rng, mu_hi=4.0)
+    prm["beta"][0] = -0.6
+    got = _gpu(bits, prm, True, True)
+    _compare(got, _ref(bits, prm, True, True), True)
+
+
 def test_dk_dv_deterministic():
     rng = np.random.default_rng(4)
     bits = {n: normal_bits(rng, (1, 2, 400, 64)) for n in ("q", "k", "v", "do")}
