@@ -816,7 +816,7 @@ __global__ void __launch_bounds__(256) bam_bwd_prep_kernel(const BwdArgs a, int 
 // dq (bf16) from the fp32 accumulator; the Delta correction of the scalar
 // sums (row blocks of one (b, h) per CTA); the last CTA writes the per-head
 // scalar gradients.
-constexpr int kFinalRows = 256;
+constexpr int kFinalRows = 256;  // = the block size: one row per thread
 
 __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
   grid_dep_wait();  // dq accumulator, row sums and scalar sums of the fused kernel
@@ -824,6 +824,24 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
   const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t nthreads = static_cast<size_t>(gridDim.x) * blockDim.x;
   if (*reinterpret_cast<volatile int*>(&a.status->abort)) return;
+  // Row blocks of kFinalRows rows (one per thread) for the Delta correction;
+  // the inputs of this CTA's first block are loaded before the dq
+  // conversion, so that their latency overlaps it.
+  const int chunks = (a.T + kFinalRows - 1) / kFinalRows;
+  const int items = a.B * a.H * chunks;
+  float4 bsum = make_float4(0.f, 0.f, 0.f, 0.f);
+  float dd = 0.f;
+  auto load_rows = [&](int item) {
+    const int i = (item % chunks) * kFinalRows + threadIdx.x;
+    bsum = make_float4(0.f, 0.f, 0.f, 0.f);
+    dd = 0.f;
+    if (i < a.T) {
+      const size_t row = static_cast<size_t>(item / chunks) * a.T + i;
+      bsum = reinterpret_cast<const float4*>(a.rowacc + row * 8)[0];
+      dd = a.delta[row] - a.rowacc[row * 8 + 4];
+    }
+  };
+  if (static_cast<int>(blockIdx.x) < items) load_rows(blockIdx.x);
   const float4* src = reinterpret_cast<const float4*>(a.dq_acc);
   uint4* dst = reinterpret_cast<uint4*>(a.dq);
   // Four groups of eight values per thread and pass, all loads issued first.
@@ -845,25 +863,12 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
                             pack_bf16x2(w[k].x, w[k].y), pack_bf16x2(w[k].z, w[k].w));
     }
   }
-  // Correction sum_i (Delta_i - C_i) B_i over this CTA's rows.
-  const int chunks = (a.T + kFinalRows - 1) / kFinalRows;
+  // Correction sum_i (Delta_i - C_i) B_i per row block, one atomic per sum.
   __shared__ float red[8][4];
   __shared__ bool last;
-  for (int item = blockIdx.x; item < a.B * a.H * chunks; item += gridDim.x) {
-    const int bh = item / chunks;
-    const int r0 = (item % chunks) * kFinalRows;
-    const int r1 = min(a.T, r0 + kFinalRows);
-    float c4[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = r0 + threadIdx.x; i < r1; i += blockDim.x) {
-      const size_t row = static_cast<size_t>(bh) * a.T + i;
-      const float4 bsum = reinterpret_cast<const float4*>(a.rowacc + row * 8)[0];
-      const float cexact = a.rowacc[row * 8 + 4];
-      const float dd = a.delta[row] - cexact;
-      c4[0] = fmaf(dd, bsum.x, c4[0]);
-      c4[1] = fmaf(dd, bsum.y, c4[1]);
-      c4[2] = fmaf(dd, bsum.z, c4[2]);
-      c4[3] = fmaf(dd, bsum.w, c4[3]);
-    }
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    if (item != static_cast<int>(blockIdx.x)) load_rows(item);
+    float c4[4] = {dd * bsum.x, dd * bsum.y, dd * bsum.z, dd * bsum.w};
 #pragma unroll
     for (int x = 0; x < 4; ++x)
 #pragma unroll
@@ -873,8 +878,8 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
     __syncthreads();
     if (threadIdx.x < 4) {
       float tot = 0.f;
-      for (int w = 0; w < 8; ++w) tot += red[w][threadIdx.x];
-      atomicAdd(a.gacc + threadIdx.x * a.H + bh % a.H, tot);
+      for (int w2 = 0; w2 < 8; ++w2) tot += red[w2][threadIdx.x];
+      atomicAdd(a.gacc + threadIdx.x * a.H + (item / chunks) % a.H, tot);
     }
     __syncthreads();
   }
