@@ -592,8 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // per CTA, 256 TMEM columns and ~107 KB of shared memory so that two CTAs
 // share an SM and overlap each other's loads, first products and O stores.
 // The K/V ring runs on across items; Q is reloaded once the item's last S
-// product has read it; O leaves through a 16 KB staging box (fp32 in two
-// passes of 32 columns).
+// product has read it; each softmax warp stages its own 32 rows of O in its
+// quarter of a 16 KB staging tile and stores them itself (fp32 in two passes
+// of 32 columns).
 constexpr int kStages1 = 2;
 constexpr int kThreads1 = 192;  // softmax warps 0-3, producer 4, MMA issuer 5
 constexpr int kWin1 = 256;      // window entries per key tile (one query tile)
