@@ -416,12 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: causal blocks with the most key tiles go first.
+  // Work item (256 query rows of one head).
   const int BH = a.B * a.H;
   const int nqb = (a.T + 255) / 256;
+  // Causal: the blocks with the most key tiles of every head first.
+  // Non-causal (all blocks alike): head by head, so that the CTAs running at
+  // the same time share their head's K and V in L2.
   const int qb = a.causal ? (nqb - 1 - static_cast<int>(blockIdx.x) / BH)
-                          : static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+                          : static_cast<int>(blockIdx.x) % nqb;
+  const int bh = a.causal ? static_cast<int>(blockIdx.x) % BH
+                          : static_cast<int>(blockIdx.x) / nqb;
   const int h = bh % a.H;
   const int i0 = qb * 256;
   const int nkv = (a.T + 127) / 128;
