@@ -115,7 +115,10 @@ bam_status bam_attn_fwd(const void* q, const void* k, const void* v, void* o, in
  * (o fp32 when o_fp32 != 0, else bf16).  Outputs: dq, dk, dv bf16
  * [B,H,T,D]; dalpha, dbeta, dmu, ds fp32 [H], overwritten, summed over the
  * batch (ds is written as 0 when ssmax == 0); with BAM_PRIOR_THETA the first
- * three are d/dtheta_alpha, d/dtheta_beta, d/dtheta_mu. */
+ * three are d/dtheta_alpha, d/dtheta_beta, d/dtheta_mu.  The call's first
+ * kernel zeroes these four and later kernels add partial sums into them with
+ * atomics (so their last bits depend on the order); after a device-side
+ * give-up they hold partial sums. */
 bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                         int o_fp32, const float* lse, const void* dO, void* dq, void* dk,
                         void* dv, float* dalpha, float* dbeta, float* dmu, float* ds, int B,

@@ -138,7 +138,7 @@ FwdWs fwd_ws(int H, int T, int causal) {
 }
 
 struct BwdWs {
-  size_t table, delta, dq_acc, rowacc, gacc, counter, total;
+  size_t table, delta, dq_acc, rowacc, total;
 };
 BwdWs bwd_ws(int B, int H, int T, int causal) {
   const TableGeom g = table_geom(T, causal);
@@ -149,9 +149,7 @@ BwdWs bwd_ws(int B, int H, int T, int causal) {
       w.table + align256((3 * kTabCopies * static_cast<size_t>(H) * g.len + kTabPadFloats) * 4);
   w.dq_acc = w.delta + align256(BH * T * 4);
   w.rowacc = w.dq_acc + align256(BH * T * kHeadDim * 4);
-  w.gacc = w.rowacc + align256(BH * T * 8 * 4);
-  w.counter = w.gacc + align256(4 * static_cast<size_t>(H) * 4);
-  w.total = w.counter + 256;
+  w.total = w.rowacc + align256(BH * T * 8 * 4);
   return w;
 }
 
@@ -453,9 +451,7 @@ bam_status bam_attn_bwd(const void* q, const void* k, const void* v, const void*
   ba.s = p->s;
   ba.delta = reinterpret_cast<float*>(wsb + w.delta);
   ba.dq_acc = reinterpret_cast<float*>(wsb + w.dq_acc);
-  ba.gacc = reinterpret_cast<float*>(wsb + w.gacc);
   ba.rowacc = reinterpret_cast<float*>(wsb + w.rowacc);
-  ba.counter = reinterpret_cast<int*>(wsb + w.counter);
   ba.dq = static_cast<uint16_t*>(dq);
   ba.dk = static_cast<uint16_t*>(dk);
   ba.dv = static_cast<uint16_t*>(dv);

@@ -119,9 +119,8 @@ struct BwdArgs {
   const float* s;
   float* delta;         // [BH, T]: rowsum(dO * O)
   float* dq_acc;        // [BH, T, 64] fp32
-  float* gacc;          // [4][H] fp32: sum dS*b, sum dS*db/dbeta, sum dS*db/dmu, sum dS*ln(n)qk/sqrt(D)
-  float* rowacc;        // [BH, T, 8]: per row sum_j P*X for the four X above, sum_j P*dP
-  int* counter;         // blocks of the final kernel that are done
+  float* rowacc;        // [BH, T, 8]: per row sum_j P*X for X = b, db/dbeta, db/dmu and
+                        // ln(n) qk/sqrt(D), then sum_j P*dP
   uint16_t* dq;         // bf16 outputs
   uint16_t* dk;
   uint16_t* dv;

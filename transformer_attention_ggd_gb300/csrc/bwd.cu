@@ -150,6 +150,26 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // (m = key, contiguous; k = query) in the 128-byte-swizzled layout: atoms of
 // 64 m-values; within an atom, row k at (k/8)*1024 + (k%8)*128 and the
 // 16-byte chunk m/8 swizzled with k%8.
+// Adds v, a partial sum of scalar-gradient term x of head h (0: sum dS b in
+// log2 units, 1: sum dS db/dbeta, 2: sum dS db/dmu, 3: the SSMax sum), to
+// that head's output, which the preprocess zeroed.  Each output is a fixed
+// multiple of its sum: d/dalpha = -(beta / alpha) ln 2 sum dS b (log2 units)
+// since db/dalpha = -beta b / alpha, or ln 2 sum dS b with the theta prior
+// (db/dtheta_alpha = b); the others are the sums themselves, and ds stays 0
+// without SSMax.
+__device__ __forceinline__ void add_head_grad(const BwdArgs& a, int x, int h, float v) {
+  if (x == 0) {
+    const float f = a.tab.prior == kPriorTheta ? kLn2f : -(__ldg(a.beta + h) / __ldg(a.alpha + h)) * kLn2f;
+    atomicAdd(a.dalpha + h, f * v);
+  } else if (x == 1) {
+    atomicAdd(a.dbeta + h, v);
+  } else if (x == 2) {
+    atomicAdd(a.dmu + h, v);
+  } else if (a.ssmax) {
+    atomicAdd(a.ds + h, v);
+  }
+}
+
 __device__ __forceinline__ uint32_t mn_chunk_offset(int m8, int k) {
   // m8: index of the 8-key chunk (0..15)
   return (m8 >> 3) * kTile + (k >> 3) * 1024 + (k & 7) * 128 + (((m8 & 7) ^ (k & 7)) << 4);
@@ -697,7 +717,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
       if (threadIdx.x < 4 && all_ok) {
         float tot = 0.f;
         for (int w = 0; w < kBCompute; ++w) tot += sm.red[round & 1][w][threadIdx.x];
-        atomicAdd(a.gacc + threadIdx.x * a.H + it.h, tot);
+        add_head_grad(a, threadIdx.x, it.h, tot);
       }
       ok = all_ok;
       if (ok) {
@@ -756,7 +776,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
 }
 
 // The three distance tables (first `table_blocks` blocks); Delta_i = dO_i .
-// O_i; zero the dq accumulator, the row sums and the scalar sums.
+// O_i; zero the dq accumulator, the row sums and the per-head gradient
+// outputs (which the later kernels add into).
 __global__ void __launch_bounds__(256) bam_bwd_prep_kernel(const BwdArgs a, int table_blocks) {
   grid_dep_trigger();
   if (static_cast<int>(blockIdx.x) < table_blocks) {
@@ -809,13 +830,17 @@ __global__ void __launch_bounds__(256) bam_bwd_prep_kernel(const BwdArgs a, int 
   for (size_t x = tid; x < n4; x += nthreads) dq4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
   float4* ra4 = reinterpret_cast<float4*>(a.rowacc);
   for (size_t x = tid; x < rows * 2; x += nthreads) ra4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (tid == 0) *a.counter = 0;
-  for (size_t x = tid; x < static_cast<size_t>(4 * a.H); x += nthreads) a.gacc[x] = 0.f;
+  for (size_t x = tid; x < static_cast<size_t>(a.H); x += nthreads) {
+    a.dalpha[x] = 0.f;
+    a.dbeta[x] = 0.f;
+    a.dmu[x] = 0.f;
+    a.ds[x] = 0.f;
+  }
 }
 
 // dq (bf16) from the fp32 accumulator; the Delta correction of the scalar
-// sums (row blocks of one (b, h) per CTA); the last CTA writes the per-head
-// scalar gradients.
+// sums (row blocks of one (b, h) per CTA), added straight into the per-head
+// gradient outputs.
 constexpr int kFinalRows = 256;  // = the block size: one row per thread
 
 __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
@@ -865,7 +890,6 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
   }
   // Correction sum_i (Delta_i - C_i) B_i per row block, one atomic per sum.
   __shared__ float red[8][4];
-  __shared__ bool last;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     if (item != static_cast<int>(blockIdx.x)) load_rows(item);
     float c4[4] = {dd * bsum.x, dd * bsum.y, dd * bsum.z, dd * bsum.w};
@@ -879,29 +903,9 @@ __global__ void __launch_bounds__(256) bam_bwd_final_kernel(const BwdArgs a) {
     if (threadIdx.x < 4) {
       float tot = 0.f;
       for (int w2 = 0; w2 < 8; ++w2) tot += red[w2][threadIdx.x];
-      atomicAdd(a.gacc + threadIdx.x * a.H + (item / chunks) % a.H, tot);
+      add_head_grad(a, threadIdx.x, (item / chunks) % a.H, tot);
     }
     __syncthreads();
-  }
-  // Last CTA: per-head outputs.  The barrier orders this CTA's atomics
-  // before thread 0's fence and count (one fence per CTA, not per thread).
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    last = (atomicAdd(a.counter, 1) == static_cast<int>(gridDim.x) - 1);
-  }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  const volatile float* g = a.gacc;
-  for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
-    const float beta = a.beta[h], alpha = a.alpha[h];
-    // sum dS * b = ln(2) * sum dS * (b log2 e).  db/dalpha = -beta b / alpha;
-    // with the theta prior db/dtheta_alpha = b.
-    a.dalpha[h] = (a.tab.prior == kPriorTheta ? 1.0f : -(beta / alpha)) * kLn2f * g[h];
-    a.dbeta[h] = g[a.H + h];
-    a.dmu[h] = g[2 * a.H + h];
-    a.ds[h] = a.ssmax ? g[3 * a.H + h] : 0.0f;
   }
 }
 
