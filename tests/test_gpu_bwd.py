@@ -108,3 +108,36 @@ def test_dk_dv_deterministic():
     np.testing.assert_array_equal(a["dv"], b["dv"])
     # dq and the scalar sums are accumulated with atomics: order may differ.
     np.testing.assert_allclose(a["dq"], b["dq"], rtol=1e-2, atol=1e-3)
+
+
+@pytest.mark.parametrize("ssmax", [True, False])
+def test_scalar_outputs_overwritten_not_accumulated(ssmax):
+    """dalpha, dbeta, dmu and ds are summed into by the kernels after the
+    call's first kernel zeroes them: outputs pre-filled with NaN come out
+    right, and a second call into the same outputs (same workspace) gives the
+    same values instead of twice them."""
+    rng = np.random.default_rng(31 + ssmax)
+    B, H, T = 2, 3, 300
+    bits = {n: normal_bits(rng, (B, H, T, 64)) for n in ("q", "k", "v", "do")}
+    prm = random_params(H, rng, mu_hi=3.0)
+    q, k, v, g = (dev_bf16(bits[n]) for n in ("q", "k", "v", "do"))
+    t = params_dev(prm)
+    o, lse = ba.attention_forward(q, k, v, t["alpha"], t["beta"], t["mu"], t["s"],
+                                  causal=True, ssmax=ssmax)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    outs = [torch.full((H,), float("nan"), dtype=torch.float32, device=q.device)
+            for _ in range(4)]
+    ws = ba.workspace(ba.BAM_OP_BWD, B, H, T, q.device)
+    p = ba.make_params(t["alpha"], t["beta"], t["mu"], t["s"], 1e-5, True, ssmax,
+                       ba.BAM_PRIOR_ALPHA)
+    ref = _ref(bits, prm, True, ssmax)
+    got = []
+    for _ in range(2):
+        ba.bam_attn_bwd(q, k, v, o, lse, g, dq, dk, dv, *outs, p, ws)
+        torch.cuda.synchronize()
+        got.append([x.cpu().numpy().copy() for x in outs])
+        res = {n: x.float().cpu().numpy() for n, x in zip(("dq", "dk", "dv"), (dq, dk, dv))}
+        res.update(zip(("dalpha", "dbeta", "dmu", "ds"), got[-1]))
+        _compare(res, ref, ssmax)
+    for a, b in zip(*got):
+        np.testing.assert_allclose(a, b, rtol=1e-4, atol=1e-6)
