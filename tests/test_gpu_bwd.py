@@ -141,3 +141,16 @@ def test_scalar_outputs_overwritten_not_accumulated(ssmax):
         _compare(res, ref, ssmax)
     for a, b in zip(*got):
         np.testing.assert_allclose(a, b, rtol=1e-4, atol=1e-6)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_long_sequence_full(causal):
+    """T = 2048 (16 key tiles, so each dQ tile is summed from up to 16
+    items): every output against the oracle, causal and not."""
+    rng = np.random.default_rng(2048 + causal)
+    B, H, T = 1, 2, 2048
+    bits = {n: normal_bits(rng, (B, H, T, 64)) for n in ("q", "k", "v", "do")}
+    prm = random_params(H, rng, mu_hi=16.0)
+    prm["beta"][0] = -0.4
+    got = _gpu(bits, prm, causal, True)
+    _compare(got, _ref(bits, prm, causal, True), True)

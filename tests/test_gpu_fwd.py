@@ -56,7 +56,7 @@ def test_small_ragged(T, causal, ssmax):
     np.testing.assert_allclose(lse, lref, rtol=LSE_RTOL, atol=LSE_ATOL)
 
 
-@pytest.mark.parametrize("T", [129, 300, 513])
+@pytest.mark.parametrize("T", [129, 300, 513, 2048])
 @pytest.mark.parametrize("causal", [True, False])
 def test_paired_and_single_tile_schedules(T, causal):
     """The forward runs 256-row CTAs (two query tiles sharing each K/V tile)
