@@ -146,10 +146,6 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
-// Byte offset of element (m, k) of a 128 x 128 bf16 MN-major operand
-// (m = key, contiguous; k = query) in the 128-byte-swizzled layout: atoms of
-// 64 m-values; within an atom, row k at (k/8)*1024 + (k%8)*128 and the
-// 16-byte chunk m/8 swizzled with k%8.
 // Adds v, a partial sum of scalar-gradient term x of head h (0: sum dS b in
 // log2 units, 1: sum dS db/dbeta, 2: sum dS db/dmu, 3: the SSMax sum), to
 // that head's output, which the preprocess zeroed.  Each output is a fixed
@@ -159,7 +155,9 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // without SSMax.
 __device__ __forceinline__ void add_head_grad(const BwdArgs& a, int x, int h, float v) {
   if (x == 0) {
-    const float f = a.tab.prior == kPriorTheta ? kLn2f : -(__ldg(a.beta + h) / __ldg(a.alpha + h)) * kLn2f;
+    const float f = a.tab.prior == kPriorTheta
+                        ? kLn2f
+                        : -(__ldg(a.beta + h) / __ldg(a.alpha + h)) * kLn2f;
     atomicAdd(a.dalpha + h, f * v);
   } else if (x == 1) {
     atomicAdd(a.dbeta + h, v);
@@ -170,6 +168,10 @@ __device__ __forceinline__ void add_head_grad(const BwdArgs& a, int x, int h, fl
   }
 }
 
+// Byte offset of element (m, k) of a 128 x 128 bf16 MN-major operand
+// (m = key, contiguous; k = query) in the 128-byte-swizzled layout: atoms of
+// 64 m-values; within an atom, row k at (k/8)*1024 + (k%8)*128 and the
+// 16-byte chunk m/8 swizzled with k%8.
 __device__ __forceinline__ uint32_t mn_chunk_offset(int m8, int k) {
   // m8: index of the 8-key chunk (0..15)
   return (m8 >> 3) * kTile + (k >> 3) * 1024 + (k & 7) * 128 + (((m8 & 7) ^ (k & 7)) << 4);
