@@ -167,7 +167,12 @@ class ClockSampler:
             self.thread.start()
         except OSError:
             self.proc = None
-        time.sleep(0.25)
+        # The timed region starts only once nvidia-smi has delivered a sample
+        # (its driver set-up done), so that set-up does not overlap the steps.
+        t0 = time.monotonic()
+        while self.proc is not None and not self.lines and time.monotonic() - t0 < 5.0:
+            time.sleep(0.01)
+        time.sleep(0.15)
         return self
 
     def _read(self):
@@ -447,6 +452,9 @@ def run_ours(args, rank, world, dev, torch, dist):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "step_ms_spread": {"min": round(min(step_ms), 5),
+                           "median": round(statistics.median(step_ms), 5),
+                           "max": round(max(step_ms), 5)},
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 tensors and per-head parameters)",
         "config": {"workload": "train_B8_H12_T512", "B": B, "H": H, "T": T, "D": D,
