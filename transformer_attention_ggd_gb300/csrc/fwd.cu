@@ -137,7 +137,7 @@ template <int W = kWin, int WS = kWinCopyStride, class Sm>
 __device__ __forceinline__ bool load_kv_tile(Sm& sm, const FwdArgs& a,
                                              const CUtensorMap* tk, const CUtensorMap* tv,
                                              int s, int j, int bh, int h, int i0, bool first,
-                                             volatile int* ab) {
+                                             volatile int* ab, bool k_before_v = false) {
   // The window of key tile j covers table indices tab_off + i0 - 128 -
   // 128 j + [0, W); in the reversed rows it starts at tab_len - W minus
   // that base (a multiple of 4 entries).  A window starts inside its own row
@@ -156,6 +156,9 @@ __device__ __forceinline__ bool load_kv_tile(Sm& sm, const FwdArgs& a,
                             tab_h + k * copy_stride + 128 * j, (W + 4) * 4, &sm.k_full[s],
                             a.table + k * copy_stride + static_cast<size_t>(h) * a.tab_len,
                             tab_end, a.status, ab, kSiteWindowCopy);
+  // The CTA's first K tile lands before its V and the next stage are
+  // requested, so that the first S product waits for Q and K only.
+  if (ok && k_before_v) ok = mbar_wait(&sm.k_full[s], 0, a.status, ab, kSiteProducer);
   mbar_arrive_expect_tx(&sm.v_full[s], kTileBytes);
   tma_load_3d(sm.v[s], tv, &sm.v_full[s], 0, 128 * j, bh);
   return ok;
@@ -712,7 +715,7 @@ __global__ void __launch_bounds__(kThreads1, 2)
             if (!ok) break;
           }
           ok = load_kv_tile<kWin1, kWin1CopyStride>(sm, a, &tk, &tv, s, j, it.bh, it.h,
-                                                     128 * it.qt, jg == 0, ab);
+                                                     128 * it.qt, jg == 0, ab, jg == 0);
         }
       }
       // Copies still in flight land before this CTA leaves.
