@@ -78,6 +78,17 @@ def load_peaks():
 
 # The files each profiled kernel is compiled from: its .cu, the headers it
 # includes, and the build script (compiler flags).
+# Cycles of the GPU spin queued ahead of the timed training steps (~2 ms at
+# 2 GHz; the host enqueues a step's flush, events and graph launch in tens of
+# microseconds).
+STEP_SPIN_CYCLES = 4_000_000
+
+# Cycles of the GPU spin that each timed call of `extra_workloads` is queued
+# behind (~0.25 ms at 2 GHz, longer than the host needs to check a call's
+# arguments and enqueue its kernels).
+CALL_SPIN_CYCLES = 500_000
+
+
 KERNEL_SOURCES = {
     "bam_bwd_kernel": ("bwd.cu", "table_eval.cuh", "bam_common.cuh", "bam_ptx.cuh"),
     "bam_fwd_kernel": ("fwd.cu", "bam_common.cuh", "bam_ptx.cuh"),
@@ -283,6 +294,10 @@ def run_ours(args, rank, world, dev, torch, dist):
     torch.cuda.synchronize()
     _nvtx(torch, "timed training steps")
     with ClockSampler(torch.cuda.current_device()) as clk:
+        # A GPU spin ahead of the steps (outside their events) lets the host
+        # enqueue all K of them before the first runs, so that a pause on the
+        # host cannot leave the GPU idle inside a step's interval.
+        torch.cuda._sleep(STEP_SPIN_CYCLES)
         for i in range(args.steps):
             flush.zero_()
             ev[i][0].record()
@@ -476,12 +491,6 @@ def run_ours(args, rank, world, dev, torch, dist):
         "clocks": clk.summary(),
     }
     return line, t
-
-
-# Cycles of the GPU spin that each timed call of `extra_workloads` is queued
-# behind (~0.25 ms at 2 GHz, longer than the host needs to check a call's
-# arguments and enqueue its kernels).
-CALL_SPIN_CYCLES = 500_000
 
 
 def gpu_call_ms(torch, call, a, b):
