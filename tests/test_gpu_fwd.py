@@ -116,10 +116,15 @@ def test_alibi_and_nope_special_cases_on_gpu():
         np.testing.assert_allclose(o, ref, rtol=0, atol=O_ATOL)
 
 
-def test_bf16_output_mode():
+@pytest.mark.parametrize("rows", [1, 160])
+def test_bf16_output_mode(rows):
+    """bf16 O against fp32 O; 160 batch rows of the same two heads run the
+    long-sequence kernel (its own bf16 staging and stores), one row the
+    short-sequence one."""
     rng = np.random.default_rng(9)
     B, H, T = 1, 2, 384
     bits = {n: normal_bits(rng, (B, H, T, 64)) for n in "qkv"}
+    bits = {n: np.ascontiguousarray(np.repeat(b, rows, axis=0)) for n, b in bits.items()}
     prm = random_params(H, rng)
     o16, lse16 = _run(bits, prm, True, True, o_dtype=torch.bfloat16)
     o32, lse32 = _run(bits, prm, True, True)

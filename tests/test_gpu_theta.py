@@ -113,6 +113,29 @@ def test_theta_forward_small_ragged(T, causal, ssmax):
     np.testing.assert_allclose(lse, lref, rtol=LSE_RTOL, atol=LSE_ATOL)
 
 
+@pytest.mark.parametrize("T", [513, 2048])
+@pytest.mark.parametrize("causal", [True, False])
+def test_theta_forward_long_sequence_kernel(T, causal):
+    """The theta prior through the long-sequence forward (256-row CTAs, which
+    run when they fill two waves of the SMs): two heads repeated over 160
+    batch rows, every row against the oracle's two heads."""
+    rng = np.random.default_rng(T + 5 * causal)
+    bits = {n: normal_bits(rng, (1, 2, T, 64)) for n in "qkv"}
+    prm = random_theta_params(2, rng)
+    prm["beta"][0] = -0.6
+    t = params_dev(prm)
+    rep = {n: dev_bf16(np.ascontiguousarray(np.repeat(b, 160, axis=0))) for n, b in bits.items()}
+    o, lse = ba.attention_forward(rep["q"], rep["k"], rep["v"], t["alpha"], t["beta"], t["mu"],
+                                  t["s"], causal=causal, ssmax=True, prior=TH)
+    torch.cuda.synchronize()
+    oref, lref = oracle.fwd(f64(bits["q"]), f64(bits["k"]), f64(bits["v"]), prm["alpha"],
+                            prm["beta"], prm["mu"], prm["s"], causal=causal, ssmax=True,
+                            prior=PRIOR_THETA)
+    o, lse = o.cpu().numpy(), lse.cpu().numpy()
+    np.testing.assert_allclose(o, np.repeat(oref, 160, axis=0), rtol=0, atol=O_ATOL)
+    np.testing.assert_allclose(lse, np.repeat(lref, 160, axis=0), rtol=LSE_RTOL, atol=LSE_ATOL)
+
+
 def _bwd_compare(bits, prm, causal, ssmax):
     t = params_dev(prm)
     q, k, v, g = (dev_bf16(bits[n]) for n in ("q", "k", "v", "do"))
