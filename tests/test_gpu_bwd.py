@@ -84,6 +84,16 @@ def test_config2_training_step_full():
     _compare(got, ref, True)
 
 
+def test_training_shape_noncausal_full():
+    """The training workload's shape without the causal mask: 384 items of
+    four query tiles each, dealt over the CTAs round-robin (several rounds),
+    every output against the oracle."""
+    d = make_inputs(2)
+    bits = {n: d[n] for n in ("q", "k", "v", "do")}
+    got = _gpu(bits, d, False, True)
+    _compare(got, _ref(bits, d, False, True), True)
+
+
 @pytest.mark.parametrize("B,H,T", [(16, 16, 512), (7, 11, 520)])
 def test_packed_schedules_full(B, H, T):
     """Shapes whose work items run in host-packed per-CTA lists (1024 items,
