@@ -25,7 +25,8 @@
 //              reversed copies each for 16-byte loads), 2 stages.
 //   warp 9     MMA issuer: S = Q K^T and dP = dO V^T (M = queries), then
 //              dV += P^T dO and dK += (c dS)^T Q (A operands MN-major in shared
-//              memory, M = keys) and dQ = (c dS) K (A = c dS from TMEM).
+//              memory, M = keys) and dQ = (c dS) K (A = the same (c dS)^T
+//              buffer read K-major: its layout is that of c dS, M = queries).
 //              S and dP of the next query tile are issued as soon as every
 //              element-wise warp has read its last S/dP columns of this one,
 //              so they overlap the end of this tile's element-wise work.
@@ -35,16 +36,16 @@
 //   warps 0-7  two warps per TMEM lane quarter; each thread owns one query
 //              row and half (64 keys) of the tile, in 16-key chunks: P, dS, the
 //              scalar-gradient sums (as f32x2 pairs of partial sums), P and
-//              c*dS to shared memory and c*dS to TMEM (each chunk stored one
-//              chunk later, so the wait for the previous tile's products
-//              overlaps arithmetic); the finished dQ tile goes to a shared
+//              c*dS to shared memory (each chunk stored one chunk later, so
+//              the wait for the previous tile's products overlaps
+//              arithmetic); the finished dQ tile goes to a shared
 //              staging tile for warp 10.  At an item's end, its dK and dV rows
 //              (TMEM lane = key) are staged as bf16 for warp 10.  Eight such
-//              warps (168 registers, no spills) measured as fast as sixteen
-//              (96 registers, spills) and leave the MMA issuer fewer busy
-//              warps on its scheduler.
-// TMEM columns: S [0,128) dP [128,256) c*dS bf16 [256,320) dQ [320,384)
-//               dK [384,448) dV [448,512).
+//              warps (168 registers, a few tens of bytes of spill stores)
+//              measured as fast as sixteen (96 registers, more spills) and
+//              leave the MMA issuer fewer busy warps on its scheduler.
+// TMEM columns: S [0,128) dP [128,256) dQ [320,384) dK [384,448)
+//               dV [448,512); [256,320) is unused.
 #include <algorithm>
 #include <climits>
 #include <mutex>
@@ -118,8 +119,7 @@ enum : int {
   kSiteBRow = 75
 };
 
-constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 320, kColDK = 384,
-                   kColDV = 448;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 320, kColDK = 384, kColDV = 448;
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, DevStatus* st,
                                           volatile int* ab, int site) {
@@ -359,6 +359,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
       const uint64_t kM = sdesc_sw128(smem_u32(sm.k), kTile, 1024);
       const uint64_t ptM = sdesc_sw128(smem_u32(sm.pt), kTile, 1024);
       const uint64_t dsM = sdesc_sw128(smem_u32(sm.dst), kTile, 1024);
+      // The same buffer read as c dS (M = queries, K = keys), K-major: its
+      // 128-byte rows are queries holding 64 keys each, swizzled by query,
+      // the second 64 keys one tile further on.
+      const uint64_t dsK = sdesc_sw128(smem_u32(sm.dst), 16, 1024);
       // S and dP of global tile g (stage g % 2) once its Q/dO are in; the
       // caller has made sure the S/dP columns are free and K/V are in.
       auto issue_s_dp = [&](int g) -> bool {
@@ -402,7 +406,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
           const uint64_t qd = qM0 + kTileDesc * s, dd = dM0 + kTileDesc * s;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ = (c dS) K
-            umma_ts(tm + kColDQ, tm + kColDS + 8 * kk, kM + 128 * kk, idQ, kk > 0 ? 1u : 0u);
+            umma_ss(tm + kColDQ, dsK + (kk >> 2) * kTileDesc + 2 * (kk & 3), kM + 128 * kk, idQ,
+                    kk > 0 ? 1u : 0u);
           if (t + 1 == it.nq) umma_commit(&sm.k_empty);  // the item's last use of K
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
@@ -566,12 +571,11 @@ __global__ void __launch_bounds__(kBThreads, 1)
         // Row partial sums for the Delta correction and the SSMax sum.
         uint64_t pB2 = 0ull, pBeta2 = 0ull, pMu2 = 0ull, pS2 = 0ull, pDP2 = 0ull, rowSS2 = 0ull;
         // P and c*dS of keys [c0, c0+8) of query row r into the MN-major
-        // operands (one 16-byte chunk each) and c*dS into TMEM.
+        // operands (one 16-byte chunk each).
         auto store_chunk = [&](int c0, const uint32_t* pp, const uint32_t* dd) {
           const uint32_t off = mn_chunk_offset(c0 / 8, r);
           *reinterpret_cast<uint4*>(sm.pt + off) = make_uint4(pp[0], pp[1], pp[2], pp[3]);
           *reinterpret_cast<uint4*>(sm.dst + off) = make_uint4(dd[0], dd[1], dd[2], dd[3]);
-          tmem_st_32x32b_x4(tm + lb + kColDS + c0 / 2, dd);
         };
         // 16-key chunks of S and dP per thread (eight independent column
         // pairs per chunk: measured 5% faster than 8-key chunks with the next
