@@ -592,11 +592,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
           uint64_t tb[8], tbeta[8], tmu[8];
           const float* wp = wv + c0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            ld_f2x2(wp + 4 * q, tb[2 * q], tb[2 * q + 1]);
-            ld_f2x2(wp + kBWinPlane + 4 * q, tbeta[2 * q], tbeta[2 * q + 1]);
-            ld_f2x2(wp + 2 * kBWinPlane + 4 * q, tmu[2 * q], tmu[2 * q + 1]);
-          }
+          for (int q = 0; q < 4; ++q) ld_f2x2(wp + 4 * q, tb[2 * q], tb[2 * q + 1]);
           tmem_ld_wait();
           reg_fence16(sv);
           reg_fence16(dpv);
@@ -611,6 +607,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
           // Masked keys (past the causal limit or T) only in chunks that reach
           // them; the test is warp-uniform so each warp takes one version.
           auto elementwise = [&](auto masked) {
+            // P and dS from the bias alone; the derivative planes are loaded
+            // after this pass and used only by the gradient sums.
+            uint64_t p2v[8], ds2v[8];
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
               const int c = c0 + 2 * x;
@@ -627,19 +626,29 @@ __global__ void __launch_bounds__(kBThreads, 1)
               const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
               const uint64_t p2 = f2_pack(p0, p1);
               const uint64_t dS2 = fmul2(p2, fadd2(dp2, ndel2));
+              p2v[x] = p2;
+              ds2v[x] = dS2;
               accB2 = ffma2(dS2, tb[x], accB2);
-              accBeta2 = ffma2(dS2, tbeta[x], accBeta2);
-              accMu2 = ffma2(dS2, tmu[x], accMu2);
               rowSS2 = ffma2(dS2, s2, rowSS2);
               pB2 = ffma2(p2, tb[x], pB2);
-              pBeta2 = ffma2(p2, tbeta[x], pBeta2);
-              pMu2 = ffma2(p2, tmu[x], pMu2);
               pS2 = ffma2(p2, s2, pS2);
               pDP2 = ffma2(p2, dp2, pDP2);
               pp[x] = pack_bf16x2(p0, p1);
               float q0, q1;
               f2_unpack(fmul2(dS2, cn2), q0, q1);
               dd[x] = pack_bf16x2(q0, q1);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              ld_f2x2(wp + kBWinPlane + 4 * q, tbeta[2 * q], tbeta[2 * q + 1]);
+              ld_f2x2(wp + 2 * kBWinPlane + 4 * q, tmu[2 * q], tmu[2 * q + 1]);
+            }
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              accBeta2 = ffma2(ds2v[x], tbeta[x], accBeta2);
+              accMu2 = ffma2(ds2v[x], tmu[x], accMu2);
+              pBeta2 = ffma2(p2v[x], tbeta[x], pBeta2);
+              pMu2 = ffma2(p2v[x], tmu[x], pMu2);
             }
           };
           if (__any_sync(0xffffffffu, c0 + kCW - 1 > lim))
