@@ -34,7 +34,8 @@
 //              into the fp32 accumulator and frees the staging tile; at an
 //              item's end, the TMA stores of its dK and dV.
 //   warps 0-7  two warps per TMEM lane quarter; each thread owns one query
-//              row and half (64 keys) of the tile, in 16-key chunks: P, dS, the
+//              row and half (64 keys) of the tile, in 16-key chunks of two
+//              passes (the derivative-table loads after P and dS): P, dS, the
 //              scalar-gradient sums (as f32x2 pairs of partial sums), P and
 //              c*dS to shared memory (each chunk stored one chunk later, so
 //              the wait for the previous tile's products overlaps
@@ -607,8 +608,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
           // Masked keys (past the causal limit or T) only in chunks that reach
           // them; the test is warp-uniform so each warp takes one version.
           auto elementwise = [&](auto masked) {
-            // P and dS from the bias alone; the derivative planes are loaded
-            // after this pass and used only by the gradient sums.
+            // Two passes: P, dS and the sums that need no derivative plane
+            // from the bias plane alone, then the two derivative planes'
+            // loads (so that a chunk's first arithmetic waits for a third of
+            // its table loads) and their four sums.
             uint64_t p2v[8], ds2v[8];
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
@@ -657,8 +660,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
             elementwise(std::false_type{});
           if (ch == 1 && t > 0) {
             // The previous tile's gradient products must be done before its
-            // P^T / dS^T buffers and dS TMEM are overwritten; its dQ tile is
-            // drained here, before this tile's dQ product is issued.  (The
+            // P^T / dS^T buffers are overwritten; its dQ tile is drained
+            // here, before this tile's dQ product is issued.  (The
             // previous item's last tile was drained at that item's end.)
             ok = warp_wait(&sm.mma_done, (g - 1) & 1, a.status, ab, kSiteBWgDone);
             if (!ok) break;
@@ -702,7 +705,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
           red_add_v4(ra, b0 + b1, e0 + e1, m0 + m1, (s0 + s1) * w_ln);
           atomicAdd(ra + 4, d0 + d1);
         }
-        tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -776,9 +778,6 @@ __global__ void __launch_bounds__(kBThreads, 1)
       }
       have = bwd_item(a, sc, round + 1, it);
     }
-    // A warp that gave up inside a tile may still have TMEM stores in
-    // flight; they complete before the columns are freed.
-    tmem_st_wait();
   }
 
   tc_fence_before();
